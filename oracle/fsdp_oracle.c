@@ -1,0 +1,358 @@
+/*
+ * fsdp_oracle.c -- plain, slow CPU oracle of the FSDP per-unit shard engine.
+ *
+ * TEST INFRASTRUCTURE. This file is the checker that the CUDA path is compared
+ * against. It shares no code, header, table or constant with the CUDA library
+ * and must never be linked into it. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline / reference leg may load it.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ * Every float operation below is a single IEEE-754 binary32 operation rounded
+ * to nearest even; nothing is contracted into an FMA or reassociated.
+ *
+ * Sources (web pages on FSDP):
+ *  [Walkthrough]   "FSDP Training Step Walkthrough": Setup, Initial state,
+ *                  Step 1.1 All-Gather, Step 4.4 Reduce-Scatter, Step 6
+ *                  Optimizer Update, per-step communication summary.
+ *  [FSDP2]         "FSDP2 的参数全聚合、梯度归约分片与显存峰值": §03 two-rank
+ *                  eight-parameter example, §09 reduce-scatter vs all-reduce.
+ *  [Tiny-FSDP]     "从源码理解 FSDP" (Tiny-FSDP walkthrough): §2.1 intra-tensor
+ *                  partition, §2.2 gather_tensor, §2.3 scatter_tensor,
+ *                  §2.4 FSDPAdamW.
+ *  [Block]         "FSDP Transformer Block Sharding Example": 4-GPU layout
+ *                  (FSDP2 per-parameter table, FSDP1 FlatParameter),
+ *                  All-Gather mechanism, FSDP1 unflatten, mixed precision
+ *                  policy (param bf16, reduce fp32).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - per-parameter shard buffers pad each parameter's segment up to a
+ *    multiple of ORC_SEG_ALIGN elements, own rows first, zeros after;
+ *  - FlatParameter: pad the flat length up to a multiple of R with zeros;
+ *  - reduction: left fold over ranks 0..R-1 starting from rank 0's value,
+ *    then one multiply by fl(1/R);
+ *  - AdamW: decoupled weight decay first, then the moment updates and the
+ *    bias-corrected step; scalars formed in double, rounded once to float.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+
+#define ORC_FLAT 1      /* FSDP1 FlatParameter */
+#define ORC_PER_PARAM 2 /* FSDP2 per-parameter Shard(0) */
+#define ORC_F32 0
+#define ORC_BF16 1
+#define ORC_SEG_ALIGN 8
+
+/* ------------------------------------------------------------------ */
+/* dim-0 ceil-div sharding ([Tiny-FSDP] §2.1; [FSDP2] §03; [Block] 4-GPU  */
+/* layout, W_Q rows 0-127 / 128-255 / 256-383 / 384-511).                */
+/* Rank r holds rows [r*s, min(r*s + s, d0)) with s = ceil(d0 / R); the  */
+/* slice is empty when r*s >= d0. Returns the row count, writes start.   */
+/* ------------------------------------------------------------------ */
+int64_t orc_rank_rows(int64_t d0, int64_t R, int64_t r, int64_t *start)
+{
+    int64_t s = (d0 + R - 1) / R;
+    int64_t begin = r * s;
+    int64_t end = begin + s;
+    if (end > d0)
+        end = d0;
+    *start = begin;
+    if (end <= begin)
+        return 0;
+    return end - begin;
+}
+
+/* ------------------------------------------------------------------ */
+/* Layout of one FSDP unit.                                           */
+/*  full_off[i]  : element offset of parameter i in the full unit      */
+/*                 (parameters concatenated row-major in unit order)  */
+/*  shard_off[i] : PER_PARAM only: offset of parameter i's segment in  */
+/*                 every rank's shard buffer                          */
+/*  shard_rows[i]: s_i = ceil(d0_i / R)                               */
+/*  out[0] = full numel P; out[1] = per-rank shard buffer numel;      */
+/*  out[2] = FLAT padded length R*S (PER_PARAM: R*out[1]).             */
+/* Returns 0, or -1 on a bad argument.                                */
+/* ------------------------------------------------------------------ */
+int orc_layout(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+               int64_t *full_off, int64_t *shard_off, int64_t *shard_rows, int64_t *out)
+{
+    if (R < 1 || n < 0 || (mode != ORC_FLAT && mode != ORC_PER_PARAM))
+        return -1;
+    int64_t total = 0;
+    int64_t seg_total = 0;
+    for (int64_t i = 0; i < n; i++) {
+        if (d0[i] < 0 || inner[i] < 0)
+            return -1;
+        full_off[i] = total;
+        total += d0[i] * inner[i];
+        int64_t s = (d0[i] + R - 1) / R;
+        shard_rows[i] = s;
+        shard_off[i] = seg_total;
+        int64_t seg = s * inner[i];
+        seg = (seg + ORC_SEG_ALIGN - 1) / ORC_SEG_ALIGN * ORC_SEG_ALIGN;
+        seg_total += seg;
+    }
+    out[0] = total;
+    if (mode == ORC_PER_PARAM) {
+        out[1] = seg_total;
+        out[2] = R * seg_total;
+    } else {
+        /* [Block] FSDP1: FlatParameter = concat(flatten(p_i)), split into
+           R equal contiguous pieces; padded with zeros to a multiple of R. */
+        int64_t S = (total + R - 1) / R;
+        out[1] = S;
+        out[2] = R * S;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* bf16 helpers. Widening is exact (bf16 is the top half of binary32).  */
+/* Narrowing is round-to-nearest-even via the usual bias trick:        */
+/* add 0x7FFF plus the lowest kept bit, then drop the low 16 bits.     */
+/* NaN maps to the quiet NaN 0x7FC0.                                   */
+/* ------------------------------------------------------------------ */
+float orc_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return 0x7fc0;
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+void orc_f32_to_bf16_array(int64_t count, const float *x, uint16_t *y)
+{
+    for (int64_t k = 0; k < count; k++)
+        y[k] = orc_f32_to_bf16(x[k]);
+}
+
+static float load_as_f32(const void *base, int dtype, int64_t idx)
+{
+    if (dtype == ORC_BF16)
+        return orc_bf16_to_f32(((const uint16_t *)base)[idx]);
+    return ((const float *)base)[idx];
+}
+
+/* ------------------------------------------------------------------ */
+/* Shard from full ([Tiny-FSDP] §2.1 partition, §4.2 "shard from full"; */
+/* [Block] FSDP1 FlatParameter ranges).                                 */
+/* full: P fp32 values in unit order. master[r]: rank r's fp32 shard    */
+/* buffer (shard numel), written with its own rows and zero padding.    */
+/* pbf16[r] (may be NULL): the bf16 copy, RNE of master.                */
+/* ------------------------------------------------------------------ */
+int orc_pack(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+             const float *full, float *const *master, uint16_t *const *pbf16)
+{
+    int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
+    if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
+        return -1;
+    int64_t P = out[0], shard_numel = out[1];
+    for (int64_t r = 0; r < R; r++) {
+        float *dst = master[r];
+        for (int64_t k = 0; k < shard_numel; k++)
+            dst[k] = 0.0f;
+        if (mode == ORC_PER_PARAM) {
+            for (int64_t i = 0; i < n; i++) {
+                int64_t start;
+                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                const float *src = full + full_off[i] + start * inner[i];
+                for (int64_t k = 0; k < cnt; k++)
+                    dst[shard_off[i] + k] = src[k];
+            }
+        } else {
+            for (int64_t k = 0; k < shard_numel; k++) {
+                int64_t j = r * shard_numel + k;
+                if (j < P)
+                    dst[k] = full[j];
+            }
+        }
+        if (pbf16 && pbf16[r])
+            orc_f32_to_bf16_array(shard_numel, dst, pbf16[r]);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* All-gather + unflatten ([Tiny-FSDP] §2.2 gather_tensor: collect all  */
+/* ranks' shards, keep the non-empty ones, concatenate along dim 0;     */
+/* [Block] All-Gather mechanism: every GPU then holds the full unit;    */
+/* FSDP1: gather the FlatParameter, drop the pad, view as parameters).  */
+/* Every one of the R destinations gets the full unit (R outputs).      */
+/* Bit copy of esize-byte elements.                                     */
+/* ------------------------------------------------------------------ */
+int orc_all_gather(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+                   int64_t esize, const void *const *shard, void *const *full)
+{
+    int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
+    if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
+        return -1;
+    int64_t P = out[0], S = out[1];
+    for (int64_t d = 0; d < R; d++) {
+        char *dst = (char *)full[d];
+        if (mode == ORC_PER_PARAM) {
+            for (int64_t i = 0; i < n; i++) {
+                /* concatenate rank 0's rows, then rank 1's, ... */
+                int64_t pos = full_off[i];
+                for (int64_t r = 0; r < R; r++) {
+                    int64_t start;
+                    int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                    if (cnt == 0)
+                        continue;
+                    const char *src = (const char *)shard[r] + shard_off[i] * esize;
+                    memcpy(dst + pos * esize, src, (size_t)(cnt * esize));
+                    pos += cnt;
+                }
+            }
+        } else {
+            int64_t pos = 0;
+            for (int64_t r = 0; r < R && pos < P; r++) {
+                int64_t cnt = P - pos < S ? P - pos : S;
+                memcpy(dst + pos * esize, shard[r], (size_t)(cnt * esize));
+                pos += cnt;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Fixed-order rank sum of `count` elements, averaged:                 */
+/*   acc = g_0[k]; acc = acc + g_1[k]; ...; acc = acc + g_{R-1}[k];     */
+/*   out[k] = acc * fl(1/R)                                            */
+/* in fp32 ([Block] mixed precision policy: reduce dtype float32;      */
+/* [Tiny-FSDP] §2.3 ReduceOp.SUM; [Walkthrough] Step 4.4 averages).     */
+/* g[q] points at rank q's values for these elements.                  */
+/* ------------------------------------------------------------------ */
+void orc_sum_ranks(int64_t R, int64_t count, int dtype, const void *const *g, float *out)
+{
+    float inv_R = 1.0f / (float)R;
+    for (int64_t k = 0; k < count; k++) {
+        float acc = load_as_f32(g[0], dtype, k);
+        for (int64_t q = 1; q < R; q++)
+            acc = acc + load_as_f32(g[q], dtype, k);
+        out[k] = acc * inv_R;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Reduce-scatter ([Tiny-FSDP] §2.3 scatter_tensor; [FSDP2] §09: the   */
+/* result equals reducing across ranks and giving segment r to rank r).*/
+/* grad[q]: rank q's full local gradient of the unit (P elements).     */
+/* gshard[r]: rank r's fp32 gradient shard in its shard-buffer layout   */
+/* (padding written as 0).                                             */
+/* ------------------------------------------------------------------ */
+int orc_reduce_scatter(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+                       int grad_dtype, const void *const *grad, float *const *gshard)
+{
+    int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
+    if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
+        return -1;
+    int64_t P = out[0], S = out[1];
+    int64_t esize = grad_dtype == ORC_BF16 ? 2 : 4;
+    const void *ptrs[R];
+    for (int64_t r = 0; r < R; r++) {
+        for (int64_t k = 0; k < S; k++)
+            gshard[r][k] = 0.0f;
+        if (mode == ORC_PER_PARAM) {
+            for (int64_t i = 0; i < n; i++) {
+                int64_t start;
+                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                int64_t j = full_off[i] + start * inner[i];
+                for (int64_t q = 0; q < R; q++)
+                    ptrs[q] = (const char *)grad[q] + j * esize;
+                orc_sum_ranks(R, cnt, grad_dtype, ptrs, gshard[r] + shard_off[i]);
+            }
+        } else {
+            int64_t j = r * S;
+            int64_t cnt = j >= P ? 0 : (P - j < S ? P - j : S);
+            for (int64_t q = 0; q < R; q++)
+                ptrs[q] = (const char *)grad[q] + j * esize;
+            orc_sum_ranks(R, cnt, grad_dtype, ptrs, gshard[r]);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* AdamW on one rank's shard ([Tiny-FSDP] §2.4 FSDPAdamW: m, v shaped  */
+/* like the local shard, zero at start, each rank updates its own shard */
+/* with no communication; [FSDP2] §04 torch.optim.AdamW).               */
+/* The update, with t >= 1 the step count:                             */
+/*   w = w * (1 - lr*wd)                                                */
+/*   m = b1*m + (1-b1)*g                                                */
+/*   v = b2*v + (1-b2)*(g*g)                                            */
+/*   w = w - (lr / (1 - b1^t)) * (m / (sqrt(v) / sqrt(1 - b2^t) + eps)) */
+/* hp = {lr, beta1, beta2, eps, weight_decay} in double.                */
+/* ------------------------------------------------------------------ */
+void orc_adamw(int64_t count, const float *g, float *w, float *m, float *v,
+               const double *hp, int64_t t)
+{
+    double lr = hp[0], beta1 = hp[1], beta2 = hp[2], eps = hp[3], wd = hp[4];
+    float decay = (float)(1.0 - lr * wd);
+    float b1 = (float)beta1;
+    float one_minus_b1 = (float)(1.0 - beta1);
+    float b2 = (float)beta2;
+    float one_minus_b2 = (float)(1.0 - beta2);
+    float step_size = (float)(lr / (1.0 - pow(beta1, (double)t)));
+    float bc2_sqrt = (float)sqrt(1.0 - pow(beta2, (double)t));
+    float epsf = (float)eps;
+    for (int64_t k = 0; k < count; k++) {
+        float gk = g[k];
+        float wk = w[k] * decay;
+        float mk = b1 * m[k] + one_minus_b1 * gk;
+        float vk = b2 * v[k] + one_minus_b2 * (gk * gk);
+        float denom = sqrtf(vk) / bc2_sqrt + epsf;
+        wk = wk - step_size * (mk / denom);
+        w[k] = wk;
+        m[k] = mk;
+        v[k] = vk;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Reduce-scatter followed by the sharded AdamW step on every rank's   */
+/* owned elements ([Walkthrough] Steps 4.4, 5, 6; [Tiny-FSDP] §2.3,     */
+/* §2.4). Padding elements are left untouched. gshard[r] (scratch that  */
+/* the caller provides, shard numel) receives the reduced gradient.     */
+/* pbf16 (may be NULL) receives RNE(w) for the whole shard buffer.      */
+/* ------------------------------------------------------------------ */
+int orc_rs_adamw(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+                 int grad_dtype, const void *const *grad, float *const *master, float *const *m,
+                 float *const *v, float *const *gshard, uint16_t *const *pbf16,
+                 const double *hp, int64_t t)
+{
+    int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
+    if (t < 1 || orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
+        return -1;
+    if (orc_reduce_scatter(mode, R, n, d0, inner, grad_dtype, grad, gshard) != 0)
+        return -1;
+    int64_t P = out[0], S = out[1];
+    for (int64_t r = 0; r < R; r++) {
+        if (mode == ORC_PER_PARAM) {
+            for (int64_t i = 0; i < n; i++) {
+                int64_t start;
+                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                int64_t o = shard_off[i];
+                orc_adamw(cnt, gshard[r] + o, master[r] + o, m[r] + o, v[r] + o, hp, t);
+            }
+        } else {
+            int64_t j = r * S;
+            int64_t cnt = j >= P ? 0 : (P - j < S ? P - j : S);
+            orc_adamw(cnt, gshard[r], master[r], m[r], v[r], hp, t);
+        }
+        if (pbf16 && pbf16[r])
+            orc_f32_to_bf16_array(S, master[r], pbf16[r]);
+    }
+    return 0;
+}
