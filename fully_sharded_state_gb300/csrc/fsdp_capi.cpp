@@ -1,0 +1,393 @@
+// fsdp_capi.cpp -- layout planner, argument validation and the extern "C"
+// entry points of the shard engine. Host code only; the kernels live in
+// fsdp_kernels.cu. Compiled with -ffp-contract=off so the AdamW scalars are
+// formed exactly as documented in fsdp_shard.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <string>
+
+#include "fsdp_internal.h"
+
+namespace fsdp {
+
+static thread_local std::string g_last_error;
+
+fsdp_status set_error(fsdp_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 60;  // byte counts (x4) stay in int64
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out)
+{
+    if (a != 0 && b > kMaxElems / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tiles of one rank piece of `len` elements.
+int64_t tiles_for(int64_t len) { return ceil_div(len, kTile); }
+
+// Split segments into launches of at most kMaxSegsPerLaunch segments, with
+// the tile numbering of each launch starting at 0. `padded` selects the
+// traversal: owned elements only (gather, reduce) or whole shard buffers
+// (pack). Segments without tiles are dropped.
+std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool padded)
+{
+    std::vector<LaunchPlan> plans;
+    LaunchPlan cur;
+    for (Seg s : segs) {
+        int64_t tiles;
+        if (padded) {
+            s.tiles_per_rank = tiles_for(s.pad_len);
+            tiles = s.tiles_per_rank * R;
+        } else {
+            if (s.numel == 0 || s.rank_stride == 0)
+                continue;
+            s.tiles_per_rank = tiles_for(s.rank_stride);
+            int64_t full_ranks = s.numel / s.rank_stride;
+            int64_t rest = s.numel - full_ranks * s.rank_stride;
+            tiles = full_ranks * s.tiles_per_rank + tiles_for(rest);
+        }
+        if (tiles == 0)
+            continue;
+        if ((int)cur.segs.size() == kMaxSegsPerLaunch) {
+            plans.push_back(cur);
+            cur = LaunchPlan();
+        }
+        s.tile_begin = cur.total_tiles;
+        cur.total_tiles += tiles;
+        cur.segs.push_back(s);
+    }
+    if (!cur.segs.empty())
+        plans.push_back(cur);
+    return plans;
+}
+
+// Rows [start, start+count) of a dim-0 extent d0 held by rank r.
+void rank_rows(int64_t d0, int R, int r, int64_t *start, int64_t *count)
+{
+    int64_t s = ceil_div(d0, R);
+    int64_t a = s * r;
+    *start = a;
+    *count = std::max<int64_t>(0, std::min<int64_t>(s, d0 - a));
+}
+
+int64_t rank_numel(const fsdp_layout_t *L, int r)
+{
+    if (L->mode == FSDP_FLAT)
+        return std::max<int64_t>(0, std::min<int64_t>(L->shard_numel, L->P - r * L->shard_numel));
+    int64_t tot = 0;
+    for (int i = 0; i < L->n; i++) {
+        int64_t a, c;
+        rank_rows(L->dim0[i], L->R, r, &a, &c);
+        tot += c * L->inner[i];
+    }
+    return tot;
+}
+
+int64_t esize(fsdp_dtype d) { return d == FSDP_BF16 ? 2 : 4; }
+
+struct Span {
+    uintptr_t lo, hi;
+    bool out;
+    const char *what;
+    int rank;
+};
+
+// Checks a host array of R device pointers. Each entry must be non-NULL
+// (when bytes > 0) and 16-byte aligned.
+fsdp_status check_ptrs(const void *const *arr, int R, int64_t bytes, bool out, const char *what,
+                       std::vector<Span> *spans)
+{
+    if (arr == nullptr)
+        return set_error(FSDP_EINVAL, "%s: pointer array is NULL", what);
+    for (int r = 0; r < R; r++) {
+        const void *p = arr[r];
+        if (bytes == 0)
+            continue;
+        if (p == nullptr)
+            return set_error(FSDP_EINVAL, "%s[%d] is NULL", what, r);
+        if (reinterpret_cast<uintptr_t>(p) & 15u)
+            return set_error(FSDP_EALIGN, "%s[%d] = %p is not 16-byte aligned", what, r, p);
+        uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        spans->push_back({lo, lo + (uintptr_t)bytes, out, what, r});
+    }
+    return FSDP_OK;
+}
+
+// Any output overlapping another buffer is an error; inputs may alias.
+fsdp_status check_overlap(std::vector<Span> &spans)
+{
+    std::sort(spans.begin(), spans.end(), [](const Span &a, const Span &b) { return a.lo < b.lo; });
+    const Span *far_any = nullptr;
+    const Span *far_out = nullptr;
+    for (const Span &s : spans) {
+        const Span *hit = nullptr;
+        if (s.out && far_any && s.lo < far_any->hi)
+            hit = far_any;
+        else if (!s.out && far_out && s.lo < far_out->hi)
+            hit = far_out;
+        if (hit)
+            return set_error(FSDP_EINVAL, "%s[%d] overlaps %s[%d]", s.what, s.rank, hit->what,
+                             hit->rank);
+        if (!far_any || s.hi > far_any->hi)
+            far_any = &s;
+        if (s.out && (!far_out || s.hi > far_out->hi))
+            far_out = &s;
+    }
+    return FSDP_OK;
+}
+
+}  // namespace
+}  // namespace fsdp
+
+using namespace fsdp;
+
+extern "C" {
+
+const char *fsdp_last_error(void) { return g_last_error.c_str(); }
+
+const char *fsdp_version(void) { return "fsdp_shard 0.1 (sm_103a)"; }
+
+fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0,
+                        const int64_t *inner, fsdp_dtype param_dtype, fsdp_dtype grad_dtype,
+                        fsdp_layout_t **out)
+{
+    if (out == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_layout: out is NULL");
+    *out = nullptr;
+    if (mode != FSDP_FLAT && mode != FSDP_PER_PARAM)
+        return set_error(FSDP_EINVAL, "fsdp_layout: unknown mode %d", (int)mode);
+    if (R < 1 || R > FSDP_MAX_RANKS)
+        return set_error(FSDP_EINVAL, "fsdp_layout: R = %d outside [1, %d]", R, FSDP_MAX_RANKS);
+    if (n_params < 0 || (n_params > 0 && (dim0 == nullptr || inner == nullptr)))
+        return set_error(FSDP_EINVAL, "fsdp_layout: bad parameter list (n_params = %d)", n_params);
+    if ((param_dtype != FSDP_F32 && param_dtype != FSDP_BF16) ||
+        (grad_dtype != FSDP_F32 && grad_dtype != FSDP_BF16))
+        return set_error(FSDP_EUNSUPPORTED, "fsdp_layout: unsupported dtype");
+
+    fsdp_layout_t *L = new (std::nothrow) fsdp_layout_t();
+    if (!L)
+        return set_error(FSDP_EINVAL, "fsdp_layout: out of host memory");
+    L->mode = mode;
+    L->R = R;
+    L->n = n_params;
+    L->param_dtype = param_dtype;
+    L->grad_dtype = grad_dtype;
+    L->dim0.assign(dim0, dim0 + n_params);
+    L->inner.assign(inner, inner + n_params);
+
+    int64_t P = 0, seg_total = 0;
+    std::vector<Seg> segs;
+    for (int i = 0; i < n_params; i++) {
+        int64_t d = dim0[i], w = inner[i], numel;
+        if (d < 0 || w < 0) {
+            delete L;
+            return set_error(FSDP_EINVAL, "fsdp_layout: parameter %d has a negative dim", i);
+        }
+        if (!mul_ok(d, w, &numel) || P > kMaxElems - numel) {
+            delete L;
+            return set_error(FSDP_ERANGE, "fsdp_layout: unit too large at parameter %d", i);
+        }
+        int64_t rows = ceil_div(d, R);
+        int64_t stride = rows * w;  // <= numel + R*w, no overflow past the check above
+        int64_t pad = ceil_div(stride, FSDP_SEG_ALIGN) * FSDP_SEG_ALIGN;
+        L->full_off.push_back(P);
+        L->shard_rows.push_back(rows);
+        L->shard_off.push_back(seg_total);
+        if (mode == FSDP_PER_PARAM)
+            segs.push_back({P, numel, stride, seg_total, pad, 0, 0});
+        P += numel;
+        seg_total += pad;
+    }
+    L->P = P;
+    if (mode == FSDP_PER_PARAM) {
+        L->shard_numel = seg_total;
+    } else {
+        int64_t S = ceil_div(P, R);
+        L->shard_numel = S;
+        segs.push_back({0, P, S, 0, S, 0, 0});
+    }
+    int64_t padded;
+    if (!mul_ok(L->shard_numel, R, &padded)) {
+        delete L;
+        return set_error(FSDP_ERANGE, "fsdp_layout: shard buffers too large");
+    }
+    L->valid_plans = make_plans(segs, R, false);
+    L->padded_plans = make_plans(segs, R, true);
+    *out = L;
+    return FSDP_OK;
+}
+
+void fsdp_layout_destroy(fsdp_layout_t *layout) { delete layout; }
+
+fsdp_status fsdp_layout_query(const fsdp_layout_t *L, fsdp_query what, int i, int r, int64_t *out)
+{
+    if (L == nullptr || out == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_layout_query: NULL argument");
+    bool need_i = what >= FSDP_Q_PARAM_FULL_OFFSET && what <= FSDP_Q_PARAM_RANK_ROWS;
+    bool need_r = what == FSDP_Q_PARAM_RANK_ROW_START || what == FSDP_Q_PARAM_RANK_ROWS ||
+                  what == FSDP_Q_RANK_NUMEL;
+    if (need_i && (i < 0 || i >= L->n))
+        return set_error(FSDP_EINVAL, "fsdp_layout_query: parameter index %d out of range", i);
+    if (need_r && (r < 0 || r >= L->R))
+        return set_error(FSDP_EINVAL, "fsdp_layout_query: rank %d out of range", r);
+    int64_t a = 0, c = 0;
+    switch (what) {
+    case FSDP_Q_FULL_NUMEL: *out = L->P; break;
+    case FSDP_Q_SHARD_NUMEL: *out = L->shard_numel; break;
+    case FSDP_Q_PADDED_NUMEL: *out = L->shard_numel * L->R; break;
+    case FSDP_Q_N_PARAMS: *out = L->n; break;
+    case FSDP_Q_RANKS: *out = L->R; break;
+    case FSDP_Q_MODE: *out = L->mode; break;
+    case FSDP_Q_PARAM_DTYPE: *out = L->param_dtype; break;
+    case FSDP_Q_GRAD_DTYPE: *out = L->grad_dtype; break;
+    case FSDP_Q_PARAM_FULL_OFFSET: *out = L->full_off[i]; break;
+    case FSDP_Q_PARAM_SHARD_OFFSET:
+        if (L->mode != FSDP_PER_PARAM)
+            return set_error(FSDP_EINVAL, "fsdp_layout_query: FLAT layouts have no per-parameter "
+                                          "shard offset");
+        *out = L->shard_off[i];
+        break;
+    case FSDP_Q_PARAM_SHARD_ROWS: *out = L->shard_rows[i]; break;
+    case FSDP_Q_PARAM_RANK_ROW_START:
+        rank_rows(L->dim0[i], L->R, r, &a, &c);
+        *out = a;
+        break;
+    case FSDP_Q_PARAM_RANK_ROWS:
+        rank_rows(L->dim0[i], L->R, r, &a, &c);
+        *out = c;
+        break;
+    case FSDP_Q_RANK_NUMEL: *out = rank_numel(L, r); break;
+    default: return set_error(FSDP_EINVAL, "fsdp_layout_query: unknown query %d", (int)what);
+    }
+    return FSDP_OK;
+}
+
+fsdp_status fsdp_pack_flat(const fsdp_layout_t *L, const float *full, void *const *param_shard,
+                           float *const *master, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_pack_flat: layout is NULL");
+    if (L->P == 0 && L->shard_numel == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    fsdp_status st;
+    if (L->P > 0) {
+        if (full == nullptr)
+            return set_error(FSDP_EINVAL, "fsdp_pack_flat: full is NULL");
+        const void *f[1] = {full};
+        if ((st = check_ptrs(f, 1, L->P * 4, false, "full", &spans)) != FSDP_OK)
+            return st;
+    }
+    if ((st = check_ptrs((const void *const *)master, L->R, L->shard_numel * 4, true, "master",
+                         &spans)) != FSDP_OK)
+        return st;
+    if (L->param_dtype == FSDP_BF16) {
+        if ((st = check_ptrs((const void *const *)param_shard, L->R, L->shard_numel * 2, true,
+                             "param_shard", &spans)) != FSDP_OK)
+            return st;
+    } else if (param_shard != nullptr) {
+        return set_error(FSDP_EINVAL, "fsdp_pack_flat: param_shard must be NULL for an F32 "
+                                      "layout (the master is the parameter shard)");
+    }
+    if ((st = check_overlap(spans)) != FSDP_OK)
+        return st;
+    return launch_pack(L, full, param_shard, master, stream);
+}
+
+fsdp_status fsdp_all_gather_unflatten(const fsdp_layout_t *L, const void *const *shard,
+                                      void *const *full_out, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_all_gather_unflatten: layout is NULL");
+    if (L->P == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    fsdp_status st;
+    int64_t es = esize(L->param_dtype);
+    if ((st = check_ptrs(shard, L->R, L->shard_numel * es, false, "shard", &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)full_out, L->R, L->P * es, true, "full_out",
+                         &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_overlap(spans)) != FSDP_OK)
+        return st;
+    return launch_all_gather(L, shard, full_out, stream);
+}
+
+fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *L, const void *const *grad_full,
+                                      float *const *master, float *const *m, float *const *v,
+                                      void *const *param_shard_out, float *const *grad_shard_out,
+                                      const fsdp_adamw_hp *hp, int64_t step, void *stream)
+{
+    if (L == nullptr || hp == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: layout or hp is NULL");
+    if (step < 1)
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: step = %lld, must be >= 1",
+                         (long long)step);
+    if (!(std::isfinite(hp->lr) && hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) ||
+        !(hp->beta2 >= 0 && hp->beta2 < 1) || !(std::isfinite(hp->eps) && hp->eps > 0) ||
+        !std::isfinite(hp->weight_decay))
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: bad hyper-parameters");
+    if (L->P == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    fsdp_status st;
+    int64_t sb = L->shard_numel * 4;
+    if ((st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
+                         &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)master, L->R, sb, true, "master", &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)m, L->R, sb, true, "m", &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)v, L->R, sb, true, "v", &spans)) != FSDP_OK)
+        return st;
+    if (L->param_dtype == FSDP_BF16) {
+        if ((st = check_ptrs((const void *const *)param_shard_out, L->R, L->shard_numel * 2, true,
+                             "param_shard_out", &spans)) != FSDP_OK)
+            return st;
+    } else if (param_shard_out != nullptr) {
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: param_shard_out must be NULL "
+                                      "for an F32 layout");
+    }
+    if (grad_shard_out != nullptr &&
+        (st = check_ptrs((const void *const *)grad_shard_out, L->R, sb, true, "grad_shard_out",
+                         &spans)) != FSDP_OK)
+        return st;
+    if ((st = check_overlap(spans)) != FSDP_OK)
+        return st;
+
+    AdamScalars c;
+    c.decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    c.b1 = (float)hp->beta1;
+    c.omb1 = (float)(1.0 - hp->beta1);
+    c.b2 = (float)hp->beta2;
+    c.omb2 = (float)(1.0 - hp->beta2);
+    c.step_size = (float)(hp->lr / (1.0 - std::pow(hp->beta1, (double)step)));
+    c.bc2_sqrt = (float)std::sqrt(1.0 - std::pow(hp->beta2, (double)step));
+    c.eps = (float)hp->eps;
+    c.inv_R = 1.0f / (float)L->R;
+    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out, c, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// fsdp_internal.h -- types shared by the library's host code (fsdp_capi.cpp)
+// and its kernels (fsdp_kernels.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "fsdp_shard.h"
+
+namespace fsdp {
+
+// Work decomposition. A tile is kTile consecutive elements of one rank's
+// piece of one segment; each thread of a CTA owns kElemsPerThread of them
+// (one 16-byte vector of bf16, two of fp32).
+constexpr int kThreads = 256;
+constexpr int kElemsPerThread = 8;
+constexpr int64_t kTile = (int64_t)kThreads * kElemsPerThread;
+// Segment descriptors travel in the kernel parameter block; larger units are
+// split into several launches.
+constexpr int kMaxSegsPerLaunch = 256;
+
+// One FSDP2 parameter, or the whole FSDP1 FlatParameter, as the kernels see
+// it. Rank r holds full elements [full_off + r*rank_stride, + n_r) with
+// n_r = clamp(numel - r*rank_stride, 0, rank_stride), stored at shard_off in
+// its shard buffer, followed by padding up to pad_len.
+struct Seg {
+    int64_t full_off;
+    int64_t numel;
+    int64_t rank_stride;
+    int64_t shard_off;
+    int64_t pad_len;
+    int64_t tile_begin;      // first tile of this segment within its launch
+    int64_t tiles_per_rank;  // tiles of a rank that holds rank_stride (or pad_len) elements
+};
+
+// The segments of one launch and its tile count.
+struct LaunchPlan {
+    std::vector<Seg> segs;
+    int64_t total_tiles = 0;
+};
+
+// AdamW scalars, formed on the host in double and rounded once to fp32.
+struct AdamScalars {
+    float decay;      // 1 - lr*wd
+    float b1, omb1;   // beta1, 1 - beta1
+    float b2, omb2;   // beta2, 1 - beta2
+    float step_size;  // lr / (1 - beta1^t)
+    float bc2_sqrt;   // sqrt(1 - beta2^t)
+    float eps;
+    float inv_R;      // fl(1/R)
+};
+
+fsdp_status set_error(fsdp_status st, const char *fmt, ...);
+
+// Kernel launchers (fsdp_kernels.cu). Arguments are validated by the caller.
+fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *param_shard,
+                        float *const *master, void *stream);
+fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
+                              void *const *full_out, void *stream);
+fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
+                            float *const *m, float *const *v, void *const *param_shard_out,
+                            float *const *grad_shard_out, const AdamScalars &c, void *stream);
+
+}  // namespace fsdp
+
+struct fsdp_layout_s {
+    fsdp_mode mode;
+    int R;
+    int n;
+    fsdp_dtype param_dtype;
+    fsdp_dtype grad_dtype;
+    std::vector<int64_t> dim0, inner, full_off, shard_off, shard_rows;
+    int64_t P;            // full numel
+    int64_t shard_numel;  // per-rank shard buffer numel
+    std::vector<fsdp::LaunchPlan> valid_plans;   // tiles over owned elements (gather, reduce)
+    std::vector<fsdp::LaunchPlan> padded_plans;  // tiles over whole shard buffers (pack)
+};

@@ -1,0 +1,580 @@
+// fsdp_kernels.cu -- the shard engine's kernels for sm_103a (GB300).
+//
+// All three kernels stream HBM: nothing here is a dense contraction, so there
+// is no tensor-core work. They share one work decomposition: a launch covers
+// up to kMaxSegsPerLaunch segments (parameters, or one FlatParameter); each
+// segment's rank pieces are cut into tiles of kTile elements; a persistent
+// grid (a few CTAs per SM) walks the tiles in order, so at any moment the
+// grid touches one contiguous window of every buffer. Each thread owns 8
+// consecutive elements of a tile: one 16-byte vector per bf16 stream, two
+// per fp32 stream. Tiles whose start is not 8-element aligned in both the
+// full and the shard buffer (ragged FSDP1 boundaries, odd row widths) take a
+// scalar path with the same per-element arithmetic.
+//
+// Segment descriptors and the R per-rank pointers travel in the kernel
+// parameter block (__grid_constant__), so the kernels need no device memory
+// beyond the caller's buffers.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "fsdp_internal.h"
+
+namespace fsdp {
+namespace {
+
+constexpr int kMaxR = FSDP_MAX_RANKS;
+
+struct PackParams {
+    const float *full;
+    float *master[kMaxR];
+    uint16_t *pshard[kMaxR];
+    int R;
+    int nseg;
+    int64_t total_tiles;
+    Seg seg[kMaxSegsPerLaunch];
+};
+
+struct GatherParams {
+    const unsigned char *shard[kMaxR];
+    unsigned char *full[kMaxR];
+    int R;
+    int nseg;
+    int64_t total_tiles;
+    Seg seg[kMaxSegsPerLaunch];
+};
+
+struct RsParams {
+    const void *grad[kMaxR];
+    float *master[kMaxR];
+    float *m[kMaxR];
+    float *v[kMaxR];
+    uint16_t *pshard[kMaxR];
+    float *gshard[kMaxR];
+    AdamScalars c;
+    int R;
+    int nseg;
+    int64_t total_tiles;
+    Seg seg[kMaxSegsPerLaunch];
+};
+
+// ---------------------------------------------------------------- tiles ----
+
+struct Tile {
+    int rank;
+    int64_t fbase;   // full-buffer index of the tile's first element
+    int64_t sbase;   // shard-buffer index of the tile's first element
+    int64_t len;     // elements in the tile
+    int64_t nvalid;  // padded traversal: elements of the tile that the rank owns
+};
+
+__device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool padded)
+{
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (seg[mid].tile_begin <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const Seg &s = seg[lo];
+    int64_t tl = t - s.tile_begin;
+    int r = (int)(tl / s.tiles_per_rank);
+    int64_t off = (tl - (int64_t)r * s.tiles_per_rank) * kTile;
+    int64_t owned = s.numel - (int64_t)r * s.rank_stride;
+    owned = owned < 0 ? 0 : (owned > s.rank_stride ? s.rank_stride : owned);
+    int64_t piece = padded ? s.pad_len : owned;
+    Tile T;
+    T.rank = r;
+    T.fbase = s.full_off + (int64_t)r * s.rank_stride + off;
+    T.sbase = s.shard_off + off;
+    T.len = piece - off < kTile ? piece - off : kTile;
+    int64_t nv = owned - off;
+    T.nvalid = nv < 0 ? 0 : (nv > T.len ? T.len : nv);
+    return T;
+}
+
+// ------------------------------------------------------ memory helpers ----
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, uint4 v)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+__device__ __forceinline__ float4 ld_f4(const float *p)
+{
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void st_f4(float *p, float4 v)
+{
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
+{
+    return __uint_as_float((uint32_t)h << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------- pack ----
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ PackParams p)
+{
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        Tile T = locate(p.seg, p.nseg, t, true);
+        float *dst = p.master[T.rank] + T.sbase;
+        const float *src = p.full + T.fbase;
+#pragma unroll
+        for (int k = 0; k < kElemsPerThread; k++) {
+            int64_t e = threadIdx.x + (int64_t)k * kThreads;
+            if (e < T.len) {
+                float x = e < T.nvalid ? src[e] : 0.0f;
+                dst[e] = x;
+                if (kBf16)
+                    p.pshard[T.rank][T.sbase + e] = f32_to_bf16_bits(x);
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------- all-gather ----------
+
+template <int kEB> struct ElemOf;
+template <> struct ElemOf<2> { using T = unsigned short; };
+template <> struct ElemOf<4> { using T = unsigned int; };
+
+// kEB = element bytes (2 for bf16, 4 for fp32); the copy is bitwise.
+template <int RC, int kEB>
+__global__ void __launch_bounds__(kThreads) all_gather_kernel(const __grid_constant__ GatherParams p)
+{
+    using E = typename ElemOf<kEB>::T;
+    const int R = RC > 0 ? RC : p.R;
+    constexpr int kVecs = kElemsPerThread * kEB / 16;  // 16-byte vectors per thread
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        Tile T = locate(p.seg, p.nseg, t, false);
+        const E *src = reinterpret_cast<const E *>(p.shard[T.rank]) + T.sbase;
+        if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0) {
+            const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+            if (e + kElemsPerThread <= T.len) {
+                uint4 x[kVecs];
+#pragma unroll
+                for (int k = 0; k < kVecs; k++)
+                    x[k] = ld_stream(src + e + k * (16 / kEB));
+                if (RC > 0) {
+#pragma unroll
+                    for (int d = 0; d < (RC > 0 ? RC : 1); d++) {
+                        E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+#pragma unroll
+                        for (int k = 0; k < kVecs; k++)
+                            st_stream(dst + k * (16 / kEB), x[k]);
+                    }
+                } else {
+                    for (int d = 0; d < R; d++) {
+                        E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+#pragma unroll
+                        for (int k = 0; k < kVecs; k++)
+                            st_stream(dst + k * (16 / kEB), x[k]);
+                    }
+                }
+                continue;
+            }
+            for (int64_t q = e; q < T.len; q++) {
+                E x = src[q];
+                for (int d = 0; d < R; d++)
+                    reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+            }
+            continue;
+        }
+#pragma unroll
+        for (int k = 0; k < kElemsPerThread; k++) {
+            int64_t q = threadIdx.x + (int64_t)k * kThreads;
+            if (q < T.len) {
+                E x = src[q];
+                for (int d = 0; d < R; d++)
+                    reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+            }
+        }
+    }
+}
+
+// ------------------------------------------- reduce-scatter + AdamW --------
+
+struct AdamOut {
+    float w, m, v;
+};
+
+// One element's AdamW step; each operation is a single fp32 operation
+// rounded to nearest even (no FMA contraction), in the documented order.
+__device__ __forceinline__ AdamOut adamw_elem(const AdamScalars &c, float g, float w, float m,
+                                              float v)
+{
+    AdamOut o;
+    float wd = __fmul_rn(w, c.decay);
+    o.m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+    o.v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+    float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(o.v), c.bc2_sqrt), c.eps);
+    o.w = __fsub_rn(wd, __fmul_rn(c.step_size, __fdiv_rn(o.m, denom)));
+    return o;
+}
+
+template <bool kGradBf16>
+__device__ __forceinline__ float load_grad(const void *g, int64_t j)
+{
+    if (kGradBf16)
+        return bf16_bits_to_f32(__ldcs(reinterpret_cast<const unsigned short *>(g) + j));
+    return __ldcs(reinterpret_cast<const float *>(g) + j);
+}
+
+// Scalar path: rank-ordered fp32 fold of element j, averaged.
+template <bool kGradBf16>
+__device__ __forceinline__ float reduce_scalar(const RsParams &p, int R, int64_t j)
+{
+    float acc = load_grad<kGradBf16>(p.grad[0], j);
+    for (int q = 1; q < R; q++)
+        acc = __fadd_rn(acc, load_grad<kGradBf16>(p.grad[q], j));
+    return __fmul_rn(acc, p.c.inv_R);
+}
+
+template <bool kGradBf16, bool kParamBf16>
+__device__ __forceinline__ void rs_adamw_scalar(const RsParams &p, int R, const Tile &T, int64_t e)
+{
+    const int r = T.rank;
+    float g = reduce_scalar<kGradBf16>(p, R, T.fbase + e);
+    int64_t s = T.sbase + e;
+    AdamOut o = adamw_elem(p.c, g, p.master[r][s], p.m[r][s], p.v[r][s]);
+    p.master[r][s] = o.w;
+    p.m[r][s] = o.m;
+    p.v[r][s] = o.v;
+    if (kParamBf16)
+        p.pshard[r][s] = f32_to_bf16_bits(o.w);
+    if (p.gshard[r])
+        p.gshard[r][s] = g;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 x, float out[8])
+{
+    out[0] = bf16_lo(x.x); out[1] = bf16_hi(x.x);
+    out[2] = bf16_lo(x.y); out[3] = bf16_hi(x.y);
+    out[4] = bf16_lo(x.z); out[5] = bf16_hi(x.z);
+    out[6] = bf16_lo(x.w); out[7] = bf16_hi(x.w);
+}
+
+// Loads the 8 gradient values of one rank at element j (8-aligned) as fp32.
+template <bool kGradBf16>
+__device__ __forceinline__ void load_grad8(const void *g, int64_t j, float out[8])
+{
+    if (kGradBf16) {
+        unpack_bf16x8(ld_stream(reinterpret_cast<const uint16_t *>(g) + j), out);
+    } else {
+        float4 a = ld_f4(reinterpret_cast<const float *>(g) + j);
+        float4 b = ld_f4(reinterpret_cast<const float *>(g) + j + 4);
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    }
+}
+
+template <int RC, bool kGradBf16, bool kParamBf16>
+__global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constant__ RsParams p)
+{
+    const int R = RC > 0 ? RC : p.R;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const Tile T = locate(p.seg, p.nseg, t, false);
+        const int r = T.rank;
+        if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
+#pragma unroll 1
+            for (int k = 0; k < kElemsPerThread; k++) {
+                int64_t e = threadIdx.x + (int64_t)k * kThreads;
+                if (e < T.len)
+                    rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, e);
+            }
+            continue;
+        }
+        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+        if (e + kElemsPerThread > T.len) {
+            for (int64_t q = e; q < T.len; q++)
+                rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, q);
+            continue;
+        }
+        const int64_t j = T.fbase + e;
+        const int64_t s = T.sbase + e;
+        // issue every load of this thread before any arithmetic
+        float acc[8];
+        float4 w0 = ld_f4(p.master[r] + s), w1 = ld_f4(p.master[r] + s + 4);
+        float4 m0 = ld_f4(p.m[r] + s), m1 = ld_f4(p.m[r] + s + 4);
+        float4 v0 = ld_f4(p.v[r] + s), v1 = ld_f4(p.v[r] + s + 4);
+        if (RC > 0 && kGradBf16) {
+            constexpr int kR = RC > 0 ? RC : 1;
+            uint4 raw[kR];
+#pragma unroll
+            for (int q = 0; q < kR; q++)
+                raw[q] = ld_stream(reinterpret_cast<const uint16_t *>(p.grad[q]) + j);
+            unpack_bf16x8(raw[0], acc);
+#pragma unroll
+            for (int q = 1; q < kR; q++) {
+                float g[8];
+                unpack_bf16x8(raw[q], g);
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    acc[k] = __fadd_rn(acc[k], g[k]);
+            }
+        } else if (RC > 0) {
+            constexpr int kR = RC > 0 ? RC : 1;
+            float g[kR][8];
+#pragma unroll
+            for (int q = 0; q < kR; q++)
+                load_grad8<kGradBf16>(p.grad[q], j, g[q]);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                float a = g[0][k];
+#pragma unroll
+                for (int q = 1; q < kR; q++)
+                    a = __fadd_rn(a, g[q][k]);
+                acc[k] = a;
+            }
+        } else {
+            load_grad8<kGradBf16>(p.grad[0], j, acc);
+            for (int q = 1; q < R; q++) {
+                float g[8];
+                load_grad8<kGradBf16>(p.grad[q], j, g);
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    acc[k] = __fadd_rn(acc[k], g[k]);
+            }
+        }
+        float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            acc[k] = __fmul_rn(acc[k], p.c.inv_R);
+            AdamOut o = adamw_elem(p.c, acc[k], wv[k], mv[k], vv[k]);
+            wv[k] = o.w;
+            mv[k] = o.m;
+            vv[k] = o.v;
+        }
+        st_f4(p.master[r] + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
+        st_f4(p.master[r] + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
+        st_f4(p.m[r] + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
+        st_f4(p.m[r] + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
+        st_f4(p.v[r] + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
+        st_f4(p.v[r] + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+        if (kParamBf16) {
+            uint4 b;
+            b.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
+            b.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
+            b.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
+            b.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
+            st_stream(p.pshard[r] + s, b);
+        }
+        if (p.gshard[r]) {
+            st_f4(p.gshard[r] + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            st_f4(p.gshard[r] + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        }
+    }
+}
+
+// ------------------------------------------------------------ launching ----
+
+struct DeviceInfo {
+    int sms = 0;
+    std::unordered_map<const void *, int> blocks_per_sm;
+};
+
+std::mutex g_dev_mu;
+std::unordered_map<int, DeviceInfo> g_dev;
+
+// Selects the device that owns `p` on this thread and returns it in *dev.
+fsdp_status select_device(const void *p, int *dev)
+{
+    cudaPointerAttributes a;
+    cudaError_t err = cudaPointerGetAttributes(&a, p);
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaPointerGetAttributes: %s", cudaGetErrorString(err));
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+        return set_error(FSDP_EINVAL, "output buffer %p is not device memory", p);
+    int cur = -1;
+    if ((err = cudaGetDevice(&cur)) != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+    if (cur != a.device && (err = cudaSetDevice(a.device)) != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaSetDevice: %s", cudaGetErrorString(err));
+    *dev = a.device;
+    return FSDP_OK;
+}
+
+// Persistent grid size for `kernel` on `dev`: resident CTAs per SM x SMs.
+fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int *grid)
+{
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    cudaError_t err;
+    if (d.sms == 0 &&
+        (err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(err));
+    auto it = d.blocks_per_sm.find(kernel);
+    if (it == d.blocks_per_sm.end()) {
+        int nb = 0;
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0)) !=
+            cudaSuccess)
+            return set_error(FSDP_ECUDA, "cudaOccupancyMaxActiveBlocksPerMultiprocessor: %s",
+                             cudaGetErrorString(err));
+        it = d.blocks_per_sm.emplace(kernel, nb < 1 ? 1 : nb).first;
+    }
+    int64_t g = (int64_t)it->second * d.sms;
+    *grid = (int)(tiles < g ? tiles : g);
+    return FSDP_OK;
+}
+
+fsdp_status check_launch(const char *what)
+{
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "%s launch failed: %s", what, cudaGetErrorString(err));
+    return FSDP_OK;
+}
+
+template <typename Params>
+void fill_segs(Params &p, const LaunchPlan &plan)
+{
+    p.nseg = (int)plan.segs.size();
+    p.total_tiles = plan.total_tiles;
+    memcpy(p.seg, plan.segs.data(), plan.segs.size() * sizeof(Seg));
+}
+
+template <typename Params, typename Kernel>
+fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const char *what)
+{
+    int grid = 0;
+    fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), p.total_tiles, &grid);
+    if (st != FSDP_OK)
+        return st;
+    kernel<<<grid, kThreads, 0, stream>>>(p);
+    return check_launch(what);
+}
+
+}  // namespace
+
+fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *param_shard,
+                        float *const *master, void *stream)
+{
+    int dev;
+    fsdp_status st = select_device(master[0], &dev);
+    if (st != FSDP_OK)
+        return st;
+    PackParams p;
+    memset(&p, 0, sizeof p);
+    p.full = full;
+    p.R = L->R;
+    for (int r = 0; r < L->R; r++) {
+        p.master[r] = master[r];
+        p.pshard[r] = param_shard ? static_cast<uint16_t *>(param_shard[r]) : nullptr;
+    }
+    for (const LaunchPlan &plan : L->padded_plans) {
+        fill_segs(p, plan);
+        st = L->param_dtype == FSDP_BF16
+                 ? run(dev, pack_kernel<true>, p, (cudaStream_t)stream, "pack")
+                 : run(dev, pack_kernel<false>, p, (cudaStream_t)stream, "pack");
+        if (st != FSDP_OK)
+            return st;
+    }
+    return FSDP_OK;
+}
+
+fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
+                              void *const *full_out, void *stream)
+{
+    int dev;
+    fsdp_status st = select_device(full_out[0], &dev);
+    if (st != FSDP_OK)
+        return st;
+    GatherParams p;
+    memset(&p, 0, sizeof p);
+    p.R = L->R;
+    for (int r = 0; r < L->R; r++) {
+        p.shard[r] = static_cast<const unsigned char *>(shard[r]);
+        p.full[r] = static_cast<unsigned char *>(full_out[r]);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = L->param_dtype == FSDP_BF16;
+    for (const LaunchPlan &plan : L->valid_plans) {
+        fill_segs(p, plan);
+        switch (bf16 ? L->R : -L->R) {
+        case 2: st = run(dev, all_gather_kernel<2, 2>, p, s, "all_gather"); break;
+        case 4: st = run(dev, all_gather_kernel<4, 2>, p, s, "all_gather"); break;
+        case 8: st = run(dev, all_gather_kernel<8, 2>, p, s, "all_gather"); break;
+        case -2: st = run(dev, all_gather_kernel<2, 4>, p, s, "all_gather"); break;
+        case -4: st = run(dev, all_gather_kernel<4, 4>, p, s, "all_gather"); break;
+        case -8: st = run(dev, all_gather_kernel<8, 4>, p, s, "all_gather"); break;
+        default:
+            st = bf16 ? run(dev, all_gather_kernel<0, 2>, p, s, "all_gather")
+                      : run(dev, all_gather_kernel<0, 4>, p, s, "all_gather");
+        }
+        if (st != FSDP_OK)
+            return st;
+    }
+    return FSDP_OK;
+}
+
+template <bool kGradBf16, bool kParamBf16>
+static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
+{
+    switch (R) {
+    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16>, p, s, "rs_adamw");
+    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16>, p, s, "rs_adamw");
+    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16>, p, s, "rs_adamw");
+    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16>, p, s, "rs_adamw");
+    }
+}
+
+fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
+                            float *const *m, float *const *v, void *const *param_shard_out,
+                            float *const *grad_shard_out, const AdamScalars &c, void *stream)
+{
+    int dev;
+    fsdp_status st = select_device(master[0], &dev);
+    if (st != FSDP_OK)
+        return st;
+    RsParams p;
+    memset(&p, 0, sizeof p);
+    p.R = L->R;
+    p.c = c;
+    for (int r = 0; r < L->R; r++) {
+        p.grad[r] = grad[r];
+        p.master[r] = master[r];
+        p.m[r] = m[r];
+        p.v[r] = v[r];
+        p.pshard[r] = param_shard_out ? static_cast<uint16_t *>(param_shard_out[r]) : nullptr;
+        p.gshard[r] = grad_shard_out ? grad_shard_out[r] : nullptr;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool gb = L->grad_dtype == FSDP_BF16, pb = L->param_dtype == FSDP_BF16;
+    for (const LaunchPlan &plan : L->valid_plans) {
+        fill_segs(p, plan);
+        if (gb && pb)
+            st = rs_dispatch<true, true>(dev, L->R, p, s);
+        else if (gb)
+            st = rs_dispatch<true, false>(dev, L->R, p, s);
+        else if (pb)
+            st = rs_dispatch<false, true>(dev, L->R, p, s);
+        else
+            st = rs_dispatch<false, false>(dev, L->R, p, s);
+        if (st != FSDP_OK)
+            return st;
+    }
+    return FSDP_OK;
+}
+
+}  // namespace fsdp

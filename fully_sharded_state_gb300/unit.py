@@ -1,0 +1,87 @@
+"""One FSDP unit sharded over R virtual ranks held in this GPU's HBM.
+
+The user-facing wrapper over the C ABI, in the spirit of wrapping one
+Transformer block as an FSDP unit ("FSDP Transformer Block Sharding
+Example", wrapping granularity): torch allocates the per-rank buffers; every
+data movement and every update runs in the CUDA library.
+
+Per rank r the unit keeps: ``master[r]`` (fp32 master shard), ``m[r]`` and
+``v[r]`` (AdamW moments, fp32, zero at start), and for bf16 parameters
+``param_shard[r]`` (the bf16 shard the all-gather reads).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import capi
+
+_DT = {"bf16": (capi.FSDP_BF16, torch.bfloat16), "f32": (capi.FSDP_F32, torch.float32)}
+_MODE = {"flat": capi.FSDP_FLAT, "per_param": capi.FSDP_PER_PARAM}
+
+
+class ShardedUnit:
+    def __init__(self, shapes, R: int, mode: str = "per_param", param_dtype: str = "bf16",
+                 grad_dtype: str = "bf16", device="cuda", names=None):
+        self.shapes = [tuple(int(x) for x in s) for s in shapes]
+        self.names = list(names) if names is not None else [f"p{i}" for i in range(len(shapes))]
+        self.R = R
+        self.mode = mode
+        self.param_dtype, self.grad_dtype = param_dtype, grad_dtype
+        self.device = torch.device(device)
+        self.layout = capi.fsdp_layout(_MODE[mode], R, self.shapes, _DT[param_dtype][0],
+                                       _DT[grad_dtype][0])
+        self.P = self.layout.full_numel
+        self.S = self.layout.shard_numel
+        z = lambda dt: [torch.zeros(self.S, dtype=dt, device=self.device) for _ in range(R)]
+        self.master = z(torch.float32)
+        self.m = z(torch.float32)
+        self.v = z(torch.float32)
+        self.param_shard = z(torch.bfloat16) if param_dtype == "bf16" else None
+        self.step = 0
+
+    # -- buffers ------------------------------------------------------------
+    @property
+    def param_torch_dtype(self):
+        return _DT[self.param_dtype][1]
+
+    @property
+    def grad_torch_dtype(self):
+        return _DT[self.grad_dtype][1]
+
+    def gather_sources(self):
+        """The shard buffers the all-gather reads (bf16 shard, or the fp32 master)."""
+        return self.param_shard if self.param_shard is not None else self.master
+
+    def alloc_full(self):
+        """R full-unit buffers in the parameter dtype (one per destination rank)."""
+        return [torch.empty(self.P, dtype=self.param_torch_dtype, device=self.device)
+                for _ in range(self.R)]
+
+    def alloc_grads(self):
+        return [torch.empty(self.P, dtype=self.grad_torch_dtype, device=self.device)
+                for _ in range(self.R)]
+
+    def unflatten(self, full) -> dict:
+        """Views of one full-unit buffer as the original parameters (no copy)."""
+        out = {}
+        for i, (name, shape) in enumerate(zip(self.names, self.shapes)):
+            off = self.layout.param_full_offset(i)
+            n = 1
+            for x in shape:
+                n *= x
+            out[name] = full[off:off + n].view(shape)
+        return out
+
+    # -- the hot path ---------------------------------------------------------
+    def shard_from_full(self, full_f32, stream=None) -> None:
+        capi.fsdp_pack_flat(self.layout, full_f32, self.param_shard, self.master, stream)
+
+    def all_gather(self, full_out, stream=None) -> None:
+        capi.fsdp_all_gather_unflatten(self.layout, self.gather_sources(), full_out, stream)
+
+    def reduce_scatter_adamw(self, grads, hp: capi.AdamWHP, grad_shard_out=None,
+                             step: int | None = None, stream=None) -> None:
+        """One optimizer step from the R ranks' full local gradients."""
+        self.step = self.step + 1 if step is None else int(step)
+        capi.fsdp_reduce_scatter_adamw(self.layout, grads, self.master, self.m, self.v,
+                                       self.param_shard, grad_shard_out, hp, self.step, stream)

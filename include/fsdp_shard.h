@@ -1,0 +1,173 @@
+/*
+ * fsdp_shard.h -- C ABI of the FSDP per-unit shard engine (GB300, sm_103a).
+ *
+ * One FSDP unit (a group of parameters gathered and reduced together, e.g.
+ * one Transformer block) is sharded over R ranks. The R ranks are virtual:
+ * each rank's buffers are separate device allocations on one GPU, and the
+ * "collectives" are the kernels below, which read and write those buffers.
+ *
+ * The operations, and where the FSDP pages define them:
+ *   fsdp_layout                dim-0 ceil-div sharding of every parameter
+ *                              ("从源码理解 FSDP", §2.1 intra-tensor partition;
+ *                              "FSDP Transformer Block Sharding Example",
+ *                              4-GPU layout: FSDP2 per-parameter table and the
+ *                              FSDP1 FlatParameter ranges).
+ *   fsdp_pack_flat             shard from full: each rank keeps its slice
+ *                              ("从源码理解 FSDP", §4.2 init_shard_from_full;
+ *                              FlatParameter = concat(flatten(p_i)), padded).
+ *   fsdp_all_gather_unflatten  every rank rebuilds the full unit from all
+ *                              shards, as the original parameter shapes
+ *                              ("从源码理解 FSDP", §2.2 gather_tensor;
+ *                              "FSDP Transformer Block Sharding Example",
+ *                              All-Gather mechanism and FSDP1 unflatten;
+ *                              "FSDP Training Step Walkthrough", Step 1.1).
+ *   fsdp_reduce_scatter_adamw  element-wise sum of the R ranks' full local
+ *                              gradients in fp32, averaged, rank r keeping its
+ *                              own slice ("从源码理解 FSDP", §2.3 scatter_tensor;
+ *                              "FSDP Training Step Walkthrough", Step 4.4;
+ *                              reduce dtype fp32 per the block page's mixed
+ *                              precision policy), fused with the sharded AdamW
+ *                              step on that slice ("从源码理解 FSDP", §2.4
+ *                              FSDPAdamW; walkthrough Step 6).
+ *
+ * Conventions (all entry points):
+ *  - Every call is host-validated first. An argument error returns a
+ *    negative status, sets the thread's fsdp_last_error() message and
+ *    launches nothing. No kernel traps or asserts.
+ *  - Kernel calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and never synchronise. The device is the one that
+ *    owns the first output buffer.
+ *  - Buffer arguments are host arrays of R device pointers, one per virtual
+ *    rank, indexed by rank. The caller owns all device memory and the
+ *    stream; the library owns only the opaque layout (host memory).
+ *  - Every device pointer must be 16-byte aligned (else FSDP_EALIGN).
+ *    Output buffers must not overlap each other or any input (else
+ *    FSDP_EINVAL); read-only inputs may alias each other.
+ *  - The full unit is the parameters concatenated row-major in unit order,
+ *    with no gaps; parameter i starts at FSDP_Q_PARAM_FULL_OFFSET(i).
+ *  - Per-rank shard buffers (FSDP_Q_SHARD_NUMEL elements each):
+ *      FSDP_PER_PARAM: parameter i occupies a segment starting at
+ *        FSDP_Q_PARAM_SHARD_OFFSET(i) of ceil(d0_i/R)*inner_i elements
+ *        rounded up to a multiple of FSDP_SEG_ALIGN; the rank's own rows come
+ *        first, zero padding after.
+ *      FSDP_FLAT: S = ceil(P/R); rank r holds flat elements [r*S, (r+1)*S)
+ *        of the unit, the part past P being zero padding.
+ *    Padding is never part of a result: the kernels do not read it and do
+ *    not write it (fsdp_pack_flat writes it as zero).
+ */
+#ifndef FSDP_SHARD_H
+#define FSDP_SHARD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FSDP_OK = 0,
+    FSDP_EINVAL = -1,       /* bad argument: NULL, count, range, aliasing */
+    FSDP_EALIGN = -2,       /* a device pointer is not 16-byte aligned */
+    FSDP_ERANGE = -3,       /* a size overflows int64 element arithmetic */
+    FSDP_ECUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+    FSDP_EUNSUPPORTED = -5  /* dtype or mode the library does not implement */
+} fsdp_status;
+
+typedef enum {
+    FSDP_FLAT = 1,      /* FSDP1: one FlatParameter per unit */
+    FSDP_PER_PARAM = 2  /* FSDP2: every parameter sharded on dim 0 */
+} fsdp_mode;
+
+typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1 } fsdp_dtype;
+
+#define FSDP_MAX_RANKS 64
+#define FSDP_SEG_ALIGN 8
+
+typedef struct fsdp_layout_s fsdp_layout_t; /* opaque; host memory */
+
+/* Build the layout of one unit of `n_params` parameters (n_params >= 0).
+ * Parameter i has shape [dim0[i], ...] with inner[i] = product of the dims
+ * after dim 0 (1 for a vector); dim0[i], inner[i] >= 0 (0 = empty
+ * parameter). 1 <= R <= FSDP_MAX_RANKS. param_dtype is the dtype of the
+ * shard buffers that the all-gather reads and of its full outputs (the fp32
+ * master is always fp32); grad_dtype is the dtype of the full local
+ * gradients. On success *out owns a new layout (free it with
+ * fsdp_layout_destroy). Errors: FSDP_EINVAL (NULL, bad R/mode/dims),
+ * FSDP_ERANGE (element counts past 2^60), FSDP_EUNSUPPORTED (dtype). */
+fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0,
+                        const int64_t *inner, fsdp_dtype param_dtype, fsdp_dtype grad_dtype,
+                        fsdp_layout_t **out);
+
+void fsdp_layout_destroy(fsdp_layout_t *layout);
+
+typedef enum {
+    FSDP_Q_FULL_NUMEL = 0,            /* P: elements of the full unit */
+    FSDP_Q_SHARD_NUMEL = 1,           /* elements of one rank's shard buffer */
+    FSDP_Q_PADDED_NUMEL = 2,          /* R * FSDP_Q_SHARD_NUMEL */
+    FSDP_Q_N_PARAMS = 3,
+    FSDP_Q_RANKS = 4,
+    FSDP_Q_MODE = 5,
+    FSDP_Q_PARAM_DTYPE = 6,
+    FSDP_Q_GRAD_DTYPE = 7,
+    FSDP_Q_PARAM_FULL_OFFSET = 8,     /* (i): offset of parameter i in the full unit */
+    FSDP_Q_PARAM_SHARD_OFFSET = 9,    /* (i): PER_PARAM segment offset; FLAT: EINVAL */
+    FSDP_Q_PARAM_SHARD_ROWS = 10,     /* (i): s_i = ceil(dim0_i / R) */
+    FSDP_Q_PARAM_RANK_ROW_START = 11, /* (i, r): first dim-0 row rank r holds */
+    FSDP_Q_PARAM_RANK_ROWS = 12,      /* (i, r): rows rank r holds (0 = empty) */
+    FSDP_Q_RANK_NUMEL = 13            /* (r): real (non-padding) elements rank r holds */
+} fsdp_query;
+
+/* Read one property of the layout into *out. `i` (parameter) and `r`
+ * (rank) are used only by the queries that name them. Errors: FSDP_EINVAL. */
+fsdp_status fsdp_layout_query(const fsdp_layout_t *layout, fsdp_query what, int i, int r,
+                              int64_t *out);
+
+/* Shard from full. `full`: device, P fp32 values of the unit. Writes, for
+ * every rank r, master[r] (fp32 shard buffer) and, when param_dtype is
+ * BF16, param_shard[r] = round-to-nearest-even bf16 of master[r]. For an
+ * F32 layout param_shard must be NULL (the master is the parameter shard).
+ * Padding is written as zero. Not on the per-step path. */
+fsdp_status fsdp_pack_flat(const fsdp_layout_t *layout, const float *full,
+                           void *const *param_shard, float *const *master, void *stream);
+
+/* All-gather + unflatten. shard[r]: rank r's parameter shard buffer in
+ * param_dtype (for F32 layouts, the fp32 master). full_out[d]: destination
+ * rank d's full unit (P elements of param_dtype). Every destination receives
+ * the same bytes: full_out[d][j] = the shard element that holds unit
+ * element j. A bit copy: no rounding. */
+fsdp_status fsdp_all_gather_unflatten(const fsdp_layout_t *layout, const void *const *shard,
+                                      void *const *full_out, void *stream);
+
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+} fsdp_adamw_hp;
+
+/* Reduce-scatter + sharded AdamW, in place on each rank's fp32 state.
+ * grad_full[q]: rank q's full local gradient of the unit (P elements of
+ * grad_dtype). For each element e that rank r owns, with j its unit index:
+ *   acc = g_0[j]; acc = acc + g_1[j]; ...; acc = acc + g_{R-1}[j]   (fp32)
+ *   g   = acc * fl(1/R)
+ *   w = w*(1 - lr*wd); m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*(g*g);
+ *   w = w - (lr/(1 - b1^step)) * (m / (sqrt(v)/sqrt(1 - b2^step) + eps))
+ * every operation an fp32 operation rounded to nearest even; the scalars
+ * are formed in double from `hp` and `step` and rounded once to fp32.
+ * master/m/v[r]: fp32 shard buffers, read and written. param_shard_out[r]:
+ * BF16 layouts only (else NULL): receives bf16 RNE of the new master.
+ * grad_shard_out: NULL, or R fp32 shard buffers that receive g (for checks;
+ * not needed for training). step >= 1; 0 <= beta1, beta2 < 1; eps > 0. */
+fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *layout, const void *const *grad_full,
+                                      float *const *master, float *const *m, float *const *v,
+                                      void *const *param_shard_out, float *const *grad_shard_out,
+                                      const fsdp_adamw_hp *hp, int64_t step, void *stream);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char *fsdp_last_error(void);
+
+/* Library version string. */
+const char *fsdp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSDP_SHARD_H */

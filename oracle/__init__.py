@@ -78,6 +78,9 @@ def _load(path: str):
     L.orc_adamw.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                             ctypes.c_void_p, ctypes.c_void_p,
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int64]
+    L.orc_owner.restype = ctypes.c_int
+    L.orc_owner.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
+                            ctypes.c_int64, _i64p, _i64p, _i64p]
     L.orc_rs_adamw.restype = ctypes.c_int
     L.orc_rs_adamw.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
                                ctypes.c_int, _vpp, _vpp, _vpp, _vpp, _vpp, _vpp,
@@ -266,3 +269,15 @@ def rs_adamw(L: Layout, grads, master, m, v, hp: AdamWHP, t: int, with_bf16: boo
                             _ptrs(p16) if p16 else _ptrs([None] * L.R), hp.as_c(), int(t))
     assert rc == 0
     return gsh, p16
+
+
+def owner(L: Layout, js) -> tuple:
+    """(rank, shard-buffer index) holding each unit element index in ``js``."""
+    js = _i64(js).ravel()
+    rank = np.zeros(js.size, np.int64)
+    index = np.zeros(js.size, np.int64)
+    rc = lib().orc_owner(L.mode, L.R, len(L.d0), _p(L.d0), _p(L.inner), js.size, _p(js),
+                         _p(rank), _p(index))
+    if rc != 0:
+        raise ValueError("oracle: element index outside the unit")
+    return rank, index

@@ -356,3 +356,43 @@ int orc_rs_adamw(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Owner of unit element j: the rank whose shard holds it and the index */
+/* inside that rank's shard buffer ([Tiny-FSDP] §2.1: rank r holds rows */
+/* [r*s, r*s+s) of every parameter; [Block] FSDP1: rank r holds flat    */
+/* elements [r*S, (r+1)*S)). Found by walking the parameters and then   */
+/* the ranks in order. Returns 0, or -1 if j is outside the unit.       */
+/* ------------------------------------------------------------------ */
+int orc_owner(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+              int64_t count, const int64_t *j, int64_t *rank, int64_t *index)
+{
+    int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
+    if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
+        return -1;
+    int64_t P = out[0], S = out[1];
+    for (int64_t k = 0; k < count; k++) {
+        int64_t e = j[k];
+        if (e < 0 || e >= P)
+            return -1;
+        if (mode == ORC_FLAT) {
+            rank[k] = e / S;
+            index[k] = e - rank[k] * S;
+            continue;
+        }
+        int64_t i = 0;
+        while (!(e >= full_off[i] && e < full_off[i] + d0[i] * inner[i]))
+            i++;
+        int64_t row = (e - full_off[i]) / inner[i];
+        for (int64_t r = 0; r < R; r++) {
+            int64_t start;
+            int64_t cnt = orc_rank_rows(d0[i], R, r, &start);
+            if (row >= start && row < start + cnt) {
+                rank[k] = r;
+                index[k] = shard_off[i] + (e - full_off[i]) - start * inner[i];
+                break;
+            }
+        }
+    }
+    return 0;
+}

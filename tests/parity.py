@@ -1,0 +1,174 @@
+"""Helpers of the GPU parity tests: run one FSDP unit through the CUDA path
+(via the C ABI) and through the CPU oracle on the same seeded inputs, and
+compare element by element.
+
+The bars:
+  - pack, all-gather and the fp32 reduce-scatter shard: bit-exact;
+  - AdamW master: |d| <= 1e-5 * max(1, |w|) per step;
+  - AdamW moments: |d| <= 1e-5 * |want| + 1e-30 (relative);
+  - bf16 parameter shard: within 1 bf16 ulp.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import oracle
+from fully_sharded_state_gb300 import AdamWHP, ShardedUnit
+from fully_sharded_state_gb300 import synth
+
+MASTER_RTOL = 1e-5
+MOMENT_RTOL = 1e-5
+BF16_ULP = 1
+
+
+def to_dev_bf16(bits: np.ndarray, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def to_dev(x: np.ndarray, device="cuda"):
+    if x.dtype == np.uint16:
+        return to_dev_bf16(x, device)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def host(t) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def bf16_ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 ulps between bit patterns (sign-magnitude ordered)."""
+    def key(u):
+        x = u.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(key(a) - key(b))
+
+
+def assert_bits_equal(got: np.ndarray, want: np.ndarray, what: str):
+    g = got.view(np.uint16 if got.dtype in (np.uint16, np.int16) else np.uint32)
+    w = want.view(np.uint16 if want.dtype in (np.uint16, np.int16) else np.uint32)
+    bad = np.flatnonzero(g != w)
+    assert bad.size == 0, f"{what}: {bad.size} of {g.size} differ, first at {bad[:5]}"
+
+
+def assert_master_close(got, want, what="master"):
+    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    bound = MASTER_RTOL * np.maximum(1.0, np.abs(want.astype(np.float64)))
+    bad = np.flatnonzero(~(err <= bound))
+    assert bad.size == 0, f"{what}: {bad.size} beyond 1e-5*max(1,|w|), first {bad[:5]}"
+
+
+def assert_moment_close(got, want, what):
+    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    bound = MOMENT_RTOL * np.abs(want.astype(np.float64)) + 1e-30
+    bad = np.flatnonzero(~(err <= bound))
+    assert bad.size == 0, f"{what}: {bad.size} beyond the relative bound, first {bad[:5]}"
+
+
+def assert_bf16_close(got, want, what="bf16 shard"):
+    d = bf16_ulp_diff(got, want)
+    assert d.max(initial=0) <= BF16_ULP, f"{what}: max {d.max()} ulp"
+
+
+@dataclass
+class UnitCase:
+    shapes: list
+    R: int
+    mode: str = "per_param"      # or "flat"
+    param_dtype: str = "bf16"
+    grad_dtype: str = "bf16"
+    seed: int = 0
+    w_std: float = 0.02
+    g_std: float = 1e-3
+    outlier_frac: float = 0.0
+    step: int = 1
+    prior_moments: bool = False
+    hp: tuple = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+
+def host_inputs(case: UnitCase):
+    P = int(sum(int(np.prod(s, dtype=np.int64)) for s in case.shapes))
+    w = synth.host_normal(1000 + case.seed, P, case.w_std)
+    grads = []
+    for r in range(case.R):
+        g = synth.host_normal(2000 + case.seed + 101 * r, P, case.g_std)
+        if case.outlier_frac:
+            mask = np.random.default_rng(3000 + case.seed + 101 * r).random(P) < case.outlier_frac
+            g[mask] *= np.float32(1e4)
+        grads.append(synth.to_bf16_bits(g) if case.grad_dtype == "bf16" else g)
+    return w, grads
+
+
+def run_unit_case(case: UnitCase, w=None, grads=None, moments=None):
+    """Pack, all-gather, reduce-scatter+AdamW, all-gather again: CUDA vs oracle."""
+    if w is None:
+        w, grads = host_inputs(case)
+    omode = oracle.FLAT if case.mode == "flat" else oracle.PER_PARAM
+    O = oracle.layout(omode, case.R, case.shapes)
+    U = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype)
+    assert (U.P, U.S) == (O.full_numel, O.shard_numel)
+    bf16 = case.param_dtype == "bf16"
+
+    # a2: shard from full
+    U.shard_from_full(to_dev(w))
+    masters, p16 = oracle.pack(O, w, with_bf16=bf16)
+    for r in range(case.R):
+        assert_bits_equal(host(U.master[r]), masters[r], f"pack master[{r}]")
+        if bf16:
+            assert_bits_equal(host(U.param_shard[r]), p16[r], f"pack bf16[{r}]")
+
+    # a3: all-gather + unflatten
+    full = U.alloc_full()
+    U.all_gather(full)
+    want_full = oracle.all_gather(O, p16 if bf16 else masters)
+    for d in range(case.R):
+        assert_bits_equal(host(full[d]), want_full[d], f"all-gather full[{d}]")
+
+    # a4-a6: reduce-scatter + AdamW
+    if moments is None and case.prior_moments:
+        wl = synth.Workload("case", case.seed, case.mode, case.R, (), case.param_dtype,
+                            case.grad_dtype, case.w_std, case.g_std)
+        moments = synth.host_moments(wl, 0, U.S)
+    m = [np.zeros(U.S, np.float32) for _ in range(case.R)]
+    v = [np.zeros(U.S, np.float32) for _ in range(case.R)]
+    if moments is not None:
+        m = [x.copy() for x in moments[0]]
+        v = [x.copy() for x in moments[1]]
+        for r in range(case.R):
+            U.m[r].copy_(to_dev(m[r]))
+            U.v[r].copy_(to_dev(v[r]))
+    lr, b1, b2, eps, wd = case.hp
+    gdev = [to_dev(g) for g in grads]
+    gsh = [torch.zeros(U.S, dtype=torch.float32, device="cuda") for _ in range(case.R)]
+    U.reduce_scatter_adamw(gdev, AdamWHP(lr, b1, b2, eps, wd), grad_shard_out=gsh,
+                           step=case.step)
+    want_g, want_p16 = oracle.rs_adamw(O, grads, masters, m, v,
+                                       oracle.AdamWHP(lr, b1, b2, eps, wd), case.step,
+                                       with_bf16=bf16)
+    exact_master = 0
+    for r in range(case.R):
+        assert_bits_equal(host(gsh[r]), want_g[r], f"reduce-scatter shard[{r}]")
+        gm = host(U.master[r])
+        assert_master_close(gm, masters[r], f"master[{r}]")
+        exact_master += int(np.sum(gm.view(np.uint32) == masters[r].view(np.uint32)))
+        assert_moment_close(host(U.m[r]), m[r], f"m[{r}]")
+        assert_moment_close(host(U.v[r]), v[r], f"v[{r}]")
+        if bf16:
+            assert_bf16_close(host(U.param_shard[r]), want_p16[r], f"bf16 shard[{r}]")
+
+    # gather of the updated shards, against the oracle's gather of its own
+    U.all_gather(full)
+    want_full = oracle.all_gather(O, want_p16 if bf16 else masters)
+    for d in range(case.R):
+        got = host(full[d])
+        if bf16:
+            assert_bf16_close(got, want_full[d], f"gather after step full[{d}]")
+        else:
+            assert_master_close(got, want_full[d], f"gather after step full[{d}]")
+    torch.cuda.synchronize()
+    return {"P": U.P, "exact_master_fraction": exact_master / max(1, case.R * U.S)}

@@ -300,6 +300,35 @@ def check_pack_matches_slicing_and_gather_restores():
                 assert np.array_equal(out, oracle.f32_to_bf16(full))
 
 
+def check_owner_matches_brute_force_and_gather():
+    """The owner of every unit element is the rank whose brute-force slice
+    holds it, and the gather reads exactly that shard slot."""
+    rng = np.random.default_rng(17)
+    for trial in range(60):
+        shapes = _tiny_shapes(rng)
+        R = int(rng.integers(1, 8))
+        P = sum(int(np.prod(s)) for s in shapes)
+        if P == 0:
+            continue
+        for mode in (oracle.PER_PARAM, oracle.FLAT):
+            L = oracle.layout(mode, R, shapes)
+            rank, index = oracle.owner(L, np.arange(P))
+            if mode == oracle.PER_PARAM:
+                ranges = brute.per_param_owner_ranges(shapes, R)
+            else:
+                S = L.shard_numel
+                ranges = [[(min(r * S, P), min((r + 1) * S, P))] for r in range(R)]
+            for r in range(R):
+                mine = [j for a, b in ranges[r] for j in range(a, b)]
+                assert np.flatnonzero(rank == r).tolist() == mine
+            # tag every shard slot with (rank, slot) and gather
+            shards = [(np.arange(L.shard_numel) + 1000 * r + 1).astype(np.float32)
+                      for r in range(R)]
+            full = oracle.all_gather(L, shards)[0]
+            want = np.array([shards[r][i] for r, i in zip(rank, index)], np.float32)
+            assert np.array_equal(full, want)
+
+
 def check_reduce_scatter_integer_sums():
     """Integer-valued gradients sum exactly in any order: the oracle's shard
     times R equals the brute-force sum for power-of-two R, and is within one

@@ -72,6 +72,11 @@ MUTANTS = [
      "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
     ("bf16 narrowing rounds half up",
      "u += 0x7fffu + keep_lsb;", "u += 0x8000u + 0u * keep_lsb;"),
+    ("owner index ignores the rank's first row",
+     "index[k] = shard_off[i] + (e - full_off[i]) - start * inner[i];",
+     "index[k] = shard_off[i] + (e - full_off[i]);"),
+    ("flat owner uses the unpadded size",
+     "rank[k] = e / S;", "rank[k] = e / (P / R > 0 ? P / R : 1); if (rank[k] >= R) rank[k] = R - 1;"),
     ("bf16 widening takes the low half",
      "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h;"),
 ]
@@ -85,8 +90,8 @@ import pins
 for check in pins.ALL_CHECKS:
     try:
         check()
-    except AssertionError:
-        print("caught by", check.__name__)
+    except Exception as exc:  # a pin that fails or errors out on the mutant
+        print("caught by", check.__name__, type(exc).__name__)
         sys.exit(3)
 print("not caught")
 sys.exit(0)

@@ -1,0 +1,108 @@
+"""Full-size parity: Llama-style decoder blocks (hidden 4096, ffn 14336, GQA),
+one FSDP unit per block, R = 8, bf16 parameters and gradients, through the
+same library calls the benchmark times (no gradient-shard output).
+
+Inputs come from the seeded device generator. The oracle computes sampled
+outputs one by one: for all-gather, the owner slot of each sampled unit
+element; for reduce-scatter + AdamW, the rank-ordered fp32 sum of the sampled
+elements' R gradients and the AdamW step on their saved state. Samples are
+uniform over the unit plus the first and last two elements of every rank
+piece of every parameter. Properties that hold at any size are checked on
+whole buffers."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fully_sharded_state_gb300 import AdamWHP, ShardedUnit, synth
+from parity import (assert_bf16_close, assert_bits_equal, assert_master_close,
+                    assert_moment_close, host)
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(O, rng, n=40000):
+    P = O.full_numel
+    js = set(rng.integers(0, P, n).tolist())
+    for i in range(len(O.shapes)):
+        for r in range(O.R):
+            s, c = O.rank_rows(i, r)
+            if c:
+                a = int(O.full_off[i] + s * O.inner[i])
+                b = a + c * int(O.inner[i])
+                js.update([a, a + 1, b - 2, b - 1])
+    js.update([0, P - 1])
+    return np.array(sorted(j for j in js if 0 <= j < P), np.int64)
+
+
+def _at(bufs, rank, idx, dev):
+    """Values of per-rank buffers at (rank[k], idx[k])."""
+    out = None
+    for r in np.unique(rank):
+        sel = np.flatnonzero(rank == r)
+        vals = host(bufs[r][torch.from_numpy(idx[sel]).to(dev)])
+        if out is None:
+            out = np.empty(rank.size, vals.dtype)
+        out[sel] = vals
+    return out
+
+
+@pytest.mark.parametrize("u", [0, 3])
+def test_llama_unit_full_size_sampled(cuda_lib, u):
+    wl = synth.WORKLOADS["llama4"]
+    dev = torch.device("cuda")
+    shapes = wl.unit_shapes(u)
+    U = ShardedUnit(shapes, wl.R, "per_param", "bf16", "bf16")
+    O = oracle.layout(oracle.PER_PARAM, wl.R, shapes)
+    assert (U.P, U.S) == (O.full_numel, O.shard_numel) == (218_112_000, 27_264_000)
+    base = synth.seed("w", wl, u)
+    for r in range(wl.R):
+        U.param_shard[r].copy_(synth.device_normal(base + r, U.S, wl.w_std, dev, torch.bfloat16))
+        U.master[r].copy_(synth.device_normal(base + 50 + r, U.S, wl.w_std, dev))
+    ms, vs = synth.device_moments(wl, u, U.S, dev)
+    for r in range(wl.R):
+        U.m[r].copy_(ms[r])
+        U.v[r].copy_(vs[r])
+    del ms, vs
+    grads = synth.device_grads(wl, u, dev)
+    rng = np.random.default_rng(100 + u)
+    js = _sample(O, rng)
+    rank, idx = oracle.owner(O, js)
+    jt = torch.from_numpy(js).to(dev)
+
+    # all-gather + unflatten
+    full = U.alloc_full()
+    U.all_gather(full)
+    want = _at(U.param_shard, rank, idx, dev)
+    for d in range(wl.R):
+        assert_bits_equal(host(full[d][jt]), want, f"full[{d}] at samples")
+    for d in range(1, wl.R):  # every destination receives the same bytes
+        assert torch.equal(full[d].view(torch.int16), full[0].view(torch.int16))
+    views = U.unflatten(full[0])
+    assert tuple(views["W_down"].shape) == (4096, 14336)
+    del full
+
+    # reduce-scatter + AdamW (step 3 with prior moments)
+    hp = AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
+    ohp = oracle.AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
+    g_s = [host(grads[q][jt]) for q in range(wl.R)]
+    w_s, m_s, v_s = (_at(b, rank, idx, dev) for b in (U.master, U.m, U.v))
+    U.reduce_scatter_adamw(grads, hp, step=3)
+    torch.cuda.synchronize()
+    gs = oracle.sum_ranks(g_s)
+    w_o, m_o, v_o = w_s.copy(), m_s.copy(), v_s.copy()
+    oracle.adamw(gs, w_o, m_o, v_o, ohp, 3)
+    assert_master_close(_at(U.master, rank, idx, dev), w_o)
+    assert_moment_close(_at(U.m, rank, idx, dev), m_o, "m")
+    assert_moment_close(_at(U.v, rank, idx, dev), v_o, "v")
+    assert_bf16_close(_at(U.param_shard, rank, idx, dev), oracle.f32_to_bf16(w_o))
+    # the bf16 shard is the rounding of the new master everywhere
+    for r in range(wl.R):
+        assert torch.equal(U.param_shard[r].view(torch.int16),
+                           U.master[r].to(torch.bfloat16).view(torch.int16))
+
+    # the reduced gradient itself, bit-exact at the samples
+    gsh = [torch.zeros(U.S, dtype=torch.float32, device=dev) for _ in range(wl.R)]
+    U.reduce_scatter_adamw(grads, hp, grad_shard_out=gsh, step=4)
+    assert_bits_equal(_at(gsh, rank, idx, dev), gs, "reduce-scatter shard at samples")
+    torch.cuda.synchronize()

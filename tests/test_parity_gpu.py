@@ -1,0 +1,142 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Every workload that the oracle finishes in seconds is run whole: the pages'
+toy, the 512/8/2048 block (FSDP2), twelve blocks as FSDP1 FlatParameters and
+the ragged stress unit; then edge cases: R = 1, odd R, the generic-R kernels,
+empty parameters and ranks, misaligned rank boundaries, more parameters than
+one launch takes, mixed dtypes, P = 0."""
+import numpy as np
+import pytest
+import torch
+
+from fully_sharded_state_gb300 import synth
+from parity import UnitCase, run_unit_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _workload_case(name, u, step=1, prior=False):
+    wl = synth.WORKLOADS[name]
+    case = UnitCase(shapes=wl.unit_shapes(u), R=wl.R, mode=wl.mode, param_dtype=wl.param_dtype,
+                    grad_dtype=wl.grad_dtype, seed=wl.cfg, w_std=wl.w_std, g_std=wl.g_std,
+                    step=step, hp=(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay))
+    w = synth.host_weights(wl, u)
+    grads = synth.host_grads(wl, u)
+    moments = None
+    if prior:
+        from fully_sharded_state_gb300 import ShardedUnit
+        S = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype).S
+        moments = synth.host_moments(wl, u, S)
+    return case, w, grads, moments
+
+
+@pytest.mark.parametrize("u", [0, 1])
+def test_toy_walkthrough_units(cuda_lib, u):
+    case, w, g, _ = _workload_case("toy", u)
+    run_unit_case(case, w, g)
+
+
+@pytest.mark.parametrize("step,prior", [(1, False), (3, True)])
+def test_block_512_fsdp2(cuda_lib, step, prior):
+    case, w, g, mom = _workload_case("block", 0, step, prior)
+    res = run_unit_case(case, w, g, mom)
+    assert res["P"] == 3_146_752
+
+
+def test_twelve_blocks_fsdp1_flat(cuda_lib):
+    for u in range(12):
+        case, w, g, mom = _workload_case("block12_flat", u, step=2, prior=True)
+        run_unit_case(case, w, g, mom)
+
+
+@pytest.mark.parametrize("step,prior", [(1, False), (2, True)])
+def test_ragged_stress(cuda_lib, step, prior):
+    case, w, g, mom = _workload_case("ragged", 0, step, prior)
+    run_unit_case(case, w, g, mom)
+
+
+EDGE = {
+    "R1": UnitCase([(37, 5), (8,)], R=1),
+    "R3_odd_average": UnitCase([(1000, 24), (7, 3)], R=3, seed=3),
+    "R5_generic": UnitCase([(513, 64), (1,)], R=5, seed=5),
+    "R9_generic_flat": UnitCase([(300, 70), (11, 13)], R=9, mode="flat", seed=9),
+    "R16_generic": UnitCase([(4097, 8)], R=16, seed=16, step=4, prior_moments=True),
+    "R64_max": UnitCase([(200, 16), (3,)], R=64, seed=64),
+    "empty_params_and_ranks": UnitCase([(0, 8), (1, 513), (3, 1), (5, 64), (0, 0), (2, 2)], R=8,
+                                       seed=11),
+    "odd_width_bf16": UnitCase([(129, 513), (127, 1)], R=4, seed=12),
+    "flat_ragged_tail": UnitCase([(1001, 3), (5, 7)], R=4, mode="flat", seed=13),
+    "flat_smaller_than_R": UnitCase([(3,)], R=8, mode="flat", seed=14),
+    "tile_edges": UnitCase([(2048, 1), (2049, 1), (2047, 1), (1, 2048 * 3 + 8)], R=2, seed=15),
+    "many_params_several_launches": UnitCase([((k * 7) % 13 + 1, 8 + (k % 3)) for k in range(600)],
+                                             R=8, seed=17),
+    "f32_params_bf16_grads": UnitCase([(256, 40), (9,)], R=4, param_dtype="f32", seed=18),
+    "bf16_params_f32_grads": UnitCase([(256, 40), (9,)], R=4, grad_dtype="f32", seed=19,
+                                      outlier_frac=0.01),
+    "f32_flat_outliers": UnitCase([(4097, 3)], R=8, mode="flat", param_dtype="f32",
+                                  grad_dtype="f32", g_std=1.0, w_std=1.0, outlier_frac=0.01,
+                                  seed=20),
+    "tiny_gradients_eps_dominated": UnitCase([(64, 64)], R=4, g_std=1e-9, seed=21),
+    "no_weight_decay_large_lr": UnitCase([(64, 64)], R=2, hp=(0.1, 0.8, 0.99, 1e-6, 0.0),
+                                         step=5, prior_moments=True, seed=22),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(cuda_lib, name):
+    run_unit_case(EDGE[name])
+
+
+def test_empty_unit_is_a_no_op(cuda_lib):
+    from fully_sharded_state_gb300 import AdamWHP, ShardedUnit
+    U = ShardedUnit([(0, 4), (0,)], R=4)
+    assert U.P == 0
+    U.all_gather(U.alloc_full())
+    U.reduce_scatter_adamw(U.alloc_grads(), AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01))
+    torch.cuda.synchronize()
+
+
+def test_side_stream(cuda_lib):
+    """Calls are asynchronous on the caller's stream."""
+    from fully_sharded_state_gb300 import ShardedUnit
+    U = ShardedUnit([(4096, 256)], R=4)
+    w = torch.randn(U.P, device="cuda")
+    s = torch.cuda.Stream()
+    full = U.alloc_full()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        U.shard_from_full(w, stream=s)
+        U.all_gather(full, stream=s)
+    s.synchronize()
+    want = w.to(torch.bfloat16)
+    for d in range(4):
+        assert torch.equal(full[d].view(torch.int16), want.view(torch.int16))
+
+
+def test_device_errors_launch_nothing(cuda_lib):
+    import ctypes
+    from fully_sharded_state_gb300 import FsdpError, ShardedUnit, capi
+    U = ShardedUnit([(64, 64)], R=2)
+    full = U.alloc_full()
+    # a bf16 view one element in: not 16-byte aligned
+    big = torch.empty(U.P + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(FsdpError) as e:
+        capi.fsdp_all_gather_unflatten(U.layout, U.gather_sources(), [big[1:U.P + 1], full[1]])
+    assert e.value.status == capi.FSDP_EALIGN
+    # two destinations that are the same buffer
+    with pytest.raises(FsdpError) as e:
+        capi.fsdp_all_gather_unflatten(U.layout, U.gather_sources(), [full[0], full[0]])
+    assert e.value.status == capi.FSDP_EINVAL
+    # output in pinned host memory is rejected before any launch
+    pinned = [torch.empty(U.P, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lib = capi.load()
+    arr_in = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in U.gather_sources()])
+    arr_out = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in pinned])
+    st = lib.fsdp_all_gather_unflatten(U.layout.handle, arr_in, arr_out, None)
+    assert st == capi.FSDP_EINVAL
+    torch.cuda.synchronize()
+
+
+def test_native_library_is_loaded(cuda_lib):
+    maps = open("/proc/self/maps").read()
+    assert "libfsdp_shard.so" in maps
