@@ -52,7 +52,7 @@ def test_llama_unit_full_size_sampled(cuda_lib, u):
     wl = synth.WORKLOADS["llama4"]
     dev = torch.device("cuda")
     shapes = wl.unit_shapes(u)
-    U = ShardedUnit(shapes, wl.R, "per_param", "bf16", "bf16")
+    U = ShardedUnit(shapes, wl.R, "per_param", "bf16", "bf16", names=[n for n, _ in wl.units[u]])
     O = oracle.layout(oracle.PER_PARAM, wl.R, shapes)
     assert (U.P, U.S) == (O.full_numel, O.shard_numel) == (218_112_000, 27_264_000)
     base = synth.seed("w", wl, u)
