@@ -390,29 +390,52 @@ def run_ours(args):
 
 
 def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
-    """The same step through the public API from host buffers: every step
-    copies each unit's R gradients from pinned host memory to the device and
-    reads the updated bf16 parameter shards back."""
+    """The same step through the public API from host buffers. Every step
+    copies each unit's R gradients from pinned host memory to the device on a
+    copy stream (each unit's copy waits only for the previous step's
+    reduce-scatter of that unit, so copies run ahead of the kernels), runs
+    the unit's all-gather and reduce-scatter + AdamW once its copy is done,
+    and reads its updated bf16 parameter shards back into pinned host memory
+    on a third stream."""
     import torch
     R = units[0].R
     P_max = max(U.P for U in units)
-    S_max = max(U.S for U in units)
     h_grads = [torch.empty(P_max, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
     for r in range(R):
         h_grads[r].copy_(grads[0][r][:P_max].cpu())
-    h_out = [torch.empty(S_max, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    h_out = [[torch.empty(U.S, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+             for U in units]
     h2d = sum(R * U.P * 2 for U in units)
     d2h = sum(R * U.S * 2 for U in units)
     steps = max(2, min(args.steps, args.e2e_steps))
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    rs_done = [torch.cuda.Event() for _ in units]
+    d2h_done = [torch.cuda.Event() for _ in units]
+    for e in rs_done + d2h_done:
+        e.record(stream)
 
     def e2e_step():
+        copied = []
         for k, U in enumerate(units):
-            for r in range(R):
-                grads[k][r].copy_(h_grads[r][:U.P], non_blocking=True)
+            h2d_stream.wait_event(rs_done[k])  # the buffer's last reader
+            with torch.cuda.stream(h2d_stream):
+                for r in range(R):
+                    grads[k][r].copy_(h_grads[r][:U.P], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(h2d_stream)
+            copied.append(e)
+        for k, U in enumerate(units):
+            stream.wait_event(copied[k])
+            stream.wait_event(d2h_done[k])  # last step's read-back of this unit's shards
             U.all_gather([f[:U.P] for f in full], stream=stream)
             U.reduce_scatter_adamw(grads[k], hp, stream=stream)
-            for r in range(R):
-                h_out[r][:U.S].copy_(U.param_shard[r], non_blocking=True)
+            rs_done[k].record(stream)
+            d2h_stream.wait_event(rs_done[k])
+            with torch.cuda.stream(d2h_stream):
+                for r in range(R):
+                    h_out[k][r].copy_(U.param_shard[r], non_blocking=True)
+            d2h_done[k].record(d2h_stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -426,8 +449,10 @@ def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
     return {"value": round(world * step_bytes * steps / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1e3 * dt / steps, 3),
-            "path": "pinned host grads -> device, all-gather, reduce-scatter+AdamW, bf16 "
-                    "shards -> pinned host, per unit, one stream"}
+            "h2d_GBps": round(h2d * steps / dt / 1e9, 1),
+            "path": "pinned host grads -> device on a copy stream running ahead, per-unit "
+                    "all-gather + reduce-scatter/AdamW on the compute stream, bf16 shards -> "
+                    "pinned host on a third stream; host wall clock"}
 
 
 def main(argv=None):

@@ -8,11 +8,12 @@ HBM. The compute path is the CUDA library ``_lib/libfsdp_shard.so``
 """
 from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, AdamWHP, FsdpError,
                    LibraryNotBuilt, fsdp_all_gather_unflatten, fsdp_layout, fsdp_pack_flat,
-                   fsdp_reduce_scatter_adamw, fsdp_version)
+                   fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_gather, fsdp_version)
 
 __all__ = ["FSDP_BF16", "FSDP_F32", "FSDP_FLAT", "FSDP_PER_PARAM", "AdamWHP", "FsdpError",
            "LibraryNotBuilt", "fsdp_all_gather_unflatten", "fsdp_layout", "fsdp_pack_flat",
-           "fsdp_reduce_scatter_adamw", "fsdp_version", "ShardedUnit"]
+           "fsdp_reduce_scatter_adamw", "fsdp_reduce_scatter_adamw_gather", "fsdp_version",
+           "ShardedUnit"]
 
 
 def __getattr__(name):

@@ -75,6 +75,11 @@ def load(path: str = LIB_PATH):
                                             ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                             ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                             ctypes.POINTER(AdamWHP), ctypes.c_int64, _vp]
+    L.fsdp_reduce_scatter_adamw_gather.restype = ctypes.c_int
+    L.fsdp_reduce_scatter_adamw_gather.argtypes = [
+        _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+        ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(AdamWHP), ctypes.c_int64,
+        _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp]
     L.fsdp_last_error.restype = ctypes.c_char_p
     L.fsdp_last_error.argtypes = []
     L.fsdp_version.restype = ctypes.c_char_p
@@ -213,6 +218,20 @@ def fsdp_reduce_scatter_adamw(layout: Layout, grad_full, master, m, v, param_sha
         _ptr_array(param_shard_out, R, "param_shard_out", allow_none=True),
         _ptr_array(grad_shard_out, R, "grad_shard_out", allow_none=True),
         ctypes.byref(hp), int(step), _stream_handle(stream)))
+
+
+def fsdp_reduce_scatter_adamw_gather(layout: Layout, grad_full, master, m, v, param_shard_out,
+                                     grad_shard_out, hp: AdamWHP, step: int,
+                                     gather_layout: Layout, shard, full_out, stream=None) -> None:
+    """Reduce-scatter + AdamW of one unit, then the all-gather of another (prefetch)."""
+    R, G = layout.R, gather_layout.R
+    _check(load().fsdp_reduce_scatter_adamw_gather(
+        layout.handle, _ptr_array(grad_full, R, "grad_full"), _ptr_array(master, R, "master"),
+        _ptr_array(m, R, "m"), _ptr_array(v, R, "v"),
+        _ptr_array(param_shard_out, R, "param_shard_out", allow_none=True),
+        _ptr_array(grad_shard_out, R, "grad_shard_out", allow_none=True),
+        ctypes.byref(hp), int(step), gather_layout.handle, _ptr_array(shard, G, "shard"),
+        _ptr_array(full_out, G, "full_out"), _stream_handle(stream)))
 
 
 def fsdp_version() -> str:

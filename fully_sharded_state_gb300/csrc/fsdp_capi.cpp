@@ -156,6 +156,75 @@ fsdp_status check_overlap(std::vector<Span> &spans)
     return FSDP_OK;
 }
 
+fsdp_status check_gather_args(const fsdp_layout_t *L, const void *const *shard,
+                              void *const *full_out, std::vector<Span> *spans)
+{
+    int64_t es = esize(L->param_dtype);
+    fsdp_status st = check_ptrs(shard, L->R, L->shard_numel * es, false, "shard", spans);
+    if (st != FSDP_OK)
+        return st;
+    return check_ptrs((const void *const *)full_out, L->R, L->P * es, true, "full_out", spans);
+}
+
+fsdp_status check_hp(const fsdp_adamw_hp *hp, int64_t step)
+{
+    if (hp == nullptr)
+        return set_error(FSDP_EINVAL, "AdamW hyper-parameters are NULL");
+    if (step < 1)
+        return set_error(FSDP_EINVAL, "step = %lld, must be >= 1", (long long)step);
+    if (!(std::isfinite(hp->lr) && hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) ||
+        !(hp->beta2 >= 0 && hp->beta2 < 1) || !(std::isfinite(hp->eps) && hp->eps > 0) ||
+        !std::isfinite(hp->weight_decay))
+        return set_error(FSDP_EINVAL, "bad AdamW hyper-parameters");
+    return FSDP_OK;
+}
+
+fsdp_status check_rs_args(const fsdp_layout_t *L, const void *const *grad_full,
+                          float *const *master, float *const *m, float *const *v,
+                          void *const *param_shard_out, float *const *grad_shard_out,
+                          std::vector<Span> *spans)
+{
+    fsdp_status st;
+    int64_t sb = L->shard_numel * 4;
+    if ((st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
+                         spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)master, L->R, sb, true, "master", spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)m, L->R, sb, true, "m", spans)) != FSDP_OK)
+        return st;
+    if ((st = check_ptrs((const void *const *)v, L->R, sb, true, "v", spans)) != FSDP_OK)
+        return st;
+    if (L->param_dtype == FSDP_BF16) {
+        if ((st = check_ptrs((const void *const *)param_shard_out, L->R, L->shard_numel * 2, true,
+                             "param_shard_out", spans)) != FSDP_OK)
+            return st;
+    } else if (param_shard_out != nullptr) {
+        return set_error(FSDP_EINVAL, "param_shard_out must be NULL for an F32 layout");
+    }
+    if (grad_shard_out != nullptr &&
+        (st = check_ptrs((const void *const *)grad_shard_out, L->R, sb, true, "grad_shard_out",
+                         spans)) != FSDP_OK)
+        return st;
+    return FSDP_OK;
+}
+
+// AdamW scalars formed in double from hp and step, rounded once to fp32.
+AdamScalars adam_scalars(const fsdp_adamw_hp *hp, int64_t step, int R)
+{
+    AdamScalars c;
+    c.decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    c.b1 = (float)hp->beta1;
+    c.omb1 = (float)(1.0 - hp->beta1);
+    c.b2 = (float)hp->beta2;
+    c.omb2 = (float)(1.0 - hp->beta2);
+    c.step_size = (float)(hp->lr / (1.0 - std::pow(hp->beta1, (double)step)));
+    c.bc2_sqrt = (float)std::sqrt(1.0 - std::pow(hp->beta2, (double)step));
+    c.eps = (float)hp->eps;
+    c.inv_R = 1.0f / (float)R;
+    return c;
+}
+
 }  // namespace
 }  // namespace fsdp
 
@@ -322,14 +391,10 @@ fsdp_status fsdp_all_gather_unflatten(const fsdp_layout_t *L, const void *const 
     if (L->P == 0)
         return FSDP_OK;
     std::vector<Span> spans;
-    fsdp_status st;
-    int64_t es = esize(L->param_dtype);
-    if ((st = check_ptrs(shard, L->R, L->shard_numel * es, false, "shard", &spans)) != FSDP_OK)
-        return st;
-    if ((st = check_ptrs((const void *const *)full_out, L->R, L->P * es, true, "full_out",
-                         &spans)) != FSDP_OK)
-        return st;
-    if ((st = check_overlap(spans)) != FSDP_OK)
+    fsdp_status st = check_gather_args(L, shard, full_out, &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
         return st;
     return launch_all_gather(L, shard, full_out, stream);
 }
@@ -339,55 +404,48 @@ fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *L, const void *const 
                                       void *const *param_shard_out, float *const *grad_shard_out,
                                       const fsdp_adamw_hp *hp, int64_t step, void *stream)
 {
-    if (L == nullptr || hp == nullptr)
-        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: layout or hp is NULL");
-    if (step < 1)
-        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: step = %lld, must be >= 1",
-                         (long long)step);
-    if (!(std::isfinite(hp->lr) && hp->lr >= 0) || !(hp->beta1 >= 0 && hp->beta1 < 1) ||
-        !(hp->beta2 >= 0 && hp->beta2 < 1) || !(std::isfinite(hp->eps) && hp->eps > 0) ||
-        !std::isfinite(hp->weight_decay))
-        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: bad hyper-parameters");
-    if (L->P == 0)
-        return FSDP_OK;
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: layout is NULL");
+    fsdp_status st = check_hp(hp, step);
+    if (st != FSDP_OK || L->P == 0)
+        return st;
     std::vector<Span> spans;
-    fsdp_status st;
-    int64_t sb = L->shard_numel * 4;
-    if ((st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
-                         &spans)) != FSDP_OK)
+    st = check_rs_args(L, grad_full, master, m, v, param_shard_out, grad_shard_out, &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
         return st;
-    if ((st = check_ptrs((const void *const *)master, L->R, sb, true, "master", &spans)) != FSDP_OK)
-        return st;
-    if ((st = check_ptrs((const void *const *)m, L->R, sb, true, "m", &spans)) != FSDP_OK)
-        return st;
-    if ((st = check_ptrs((const void *const *)v, L->R, sb, true, "v", &spans)) != FSDP_OK)
-        return st;
-    if (L->param_dtype == FSDP_BF16) {
-        if ((st = check_ptrs((const void *const *)param_shard_out, L->R, L->shard_numel * 2, true,
-                             "param_shard_out", &spans)) != FSDP_OK)
-            return st;
-    } else if (param_shard_out != nullptr) {
-        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw: param_shard_out must be NULL "
-                                      "for an F32 layout");
-    }
-    if (grad_shard_out != nullptr &&
-        (st = check_ptrs((const void *const *)grad_shard_out, L->R, sb, true, "grad_shard_out",
-                         &spans)) != FSDP_OK)
-        return st;
-    if ((st = check_overlap(spans)) != FSDP_OK)
-        return st;
+    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                           adam_scalars(hp, step, L->R), stream);
+}
 
-    AdamScalars c;
-    c.decay = (float)(1.0 - hp->lr * hp->weight_decay);
-    c.b1 = (float)hp->beta1;
-    c.omb1 = (float)(1.0 - hp->beta1);
-    c.b2 = (float)hp->beta2;
-    c.omb2 = (float)(1.0 - hp->beta2);
-    c.step_size = (float)(hp->lr / (1.0 - std::pow(hp->beta1, (double)step)));
-    c.bc2_sqrt = (float)std::sqrt(1.0 - std::pow(hp->beta2, (double)step));
-    c.eps = (float)hp->eps;
-    c.inv_R = 1.0f / (float)L->R;
-    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out, c, stream);
+fsdp_status fsdp_reduce_scatter_adamw_gather(
+    const fsdp_layout_t *L, const void *const *grad_full, float *const *master, float *const *m,
+    float *const *v, void *const *param_shard_out, float *const *grad_shard_out,
+    const fsdp_adamw_hp *hp, int64_t step, const fsdp_layout_t *G, const void *const *shard,
+    void *const *full_out, void *stream)
+{
+    if (L == nullptr || G == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw_gather: layout is NULL");
+    fsdp_status st = check_hp(hp, step);
+    if (st != FSDP_OK)
+        return st;
+    std::vector<Span> spans;
+    if (L->P > 0)
+        st = check_rs_args(L, grad_full, master, m, v, param_shard_out, grad_shard_out, &spans);
+    if (st == FSDP_OK && G->P > 0)
+        st = check_gather_args(G, shard, full_out, &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
+        return st;
+    if (L->P == 0)
+        return G->P == 0 ? FSDP_OK : launch_all_gather(G, shard, full_out, stream);
+    if (G->P == 0)
+        return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                               adam_scalars(hp, step, L->R), stream);
+    return launch_rs_adamw_gather(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                                  adam_scalars(hp, step, L->R), G, shard, full_out, stream);
 }
 
 }  // extern "C"

@@ -29,6 +29,17 @@ namespace {
 
 constexpr int kMaxR = FSDP_MAX_RANKS;
 
+// Resident CTAs per SM of each kernel's persistent grid. Measured on GB300
+// with 218M-parameter Llama units, R = 8 (one launch per point):
+//   reduce-scatter + AdamW: 2/SM 1.520 ms, 3/SM 1.389 ms, 4/SM (the register
+//   limit) 1.498 ms;  all-gather: 2/SM 0.655 ms, 3/SM 0.690 ms, 8/SM (the
+//   limit) 0.690 ms.
+// Fewer CTAs, each streaming its tiles in order, keep a narrower window of
+// every buffer open at once; past these points HBM does not go faster.
+constexpr int kRsCtasPerSm = 3;
+constexpr int kGatherCtasPerSm = 2;
+constexpr int kPackCtasPerSm = 8;
+
 struct PackParams {
     const float *full;
     float *master[kMaxR];
@@ -157,58 +168,64 @@ template <int kEB> struct ElemOf;
 template <> struct ElemOf<2> { using T = unsigned short; };
 template <> struct ElemOf<4> { using T = unsigned int; };
 
-// kEB = element bytes (2 for bf16, 4 for fp32); the copy is bitwise.
+// One all-gather tile: the tile's shard elements go to the same place of
+// every destination's full buffer. kEB = element bytes (2 bf16, 4 fp32); the
+// copy is bitwise. PP is any parameter block with `shard` and `full`.
+template <int RC, int kEB, class PP>
+__device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
+{
+    using E = typename ElemOf<kEB>::T;
+    constexpr int kVecs = kElemsPerThread * kEB / 16;  // 16-byte vectors per thread
+    const E *src = reinterpret_cast<const E *>(p.shard[T.rank]) + T.sbase;
+    if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0) {
+        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+        if (e + kElemsPerThread <= T.len) {
+            uint4 x[kVecs];
+#pragma unroll
+            for (int k = 0; k < kVecs; k++)
+                x[k] = ld_stream(src + e + k * (16 / kEB));
+            if (RC > 0) {
+#pragma unroll
+                for (int d = 0; d < (RC > 0 ? RC : 1); d++) {
+                    E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+#pragma unroll
+                    for (int k = 0; k < kVecs; k++)
+                        st_stream(dst + k * (16 / kEB), x[k]);
+                }
+            } else {
+                for (int d = 0; d < R; d++) {
+                    E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+#pragma unroll
+                    for (int k = 0; k < kVecs; k++)
+                        st_stream(dst + k * (16 / kEB), x[k]);
+                }
+            }
+            return;
+        }
+        for (int64_t q = e; q < T.len; q++) {
+            E x = src[q];
+            for (int d = 0; d < R; d++)
+                reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+        }
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < kElemsPerThread; k++) {
+        int64_t q = threadIdx.x + (int64_t)k * kThreads;
+        if (q < T.len) {
+            E x = src[q];
+            for (int d = 0; d < R; d++)
+                reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+        }
+    }
+}
+
 template <int RC, int kEB>
 __global__ void __launch_bounds__(kThreads) all_gather_kernel(const __grid_constant__ GatherParams p)
 {
-    using E = typename ElemOf<kEB>::T;
     const int R = RC > 0 ? RC : p.R;
-    constexpr int kVecs = kElemsPerThread * kEB / 16;  // 16-byte vectors per thread
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        Tile T = locate(p.seg, p.nseg, t, false);
-        const E *src = reinterpret_cast<const E *>(p.shard[T.rank]) + T.sbase;
-        if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0) {
-            const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
-            if (e + kElemsPerThread <= T.len) {
-                uint4 x[kVecs];
-#pragma unroll
-                for (int k = 0; k < kVecs; k++)
-                    x[k] = ld_stream(src + e + k * (16 / kEB));
-                if (RC > 0) {
-#pragma unroll
-                    for (int d = 0; d < (RC > 0 ? RC : 1); d++) {
-                        E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
-#pragma unroll
-                        for (int k = 0; k < kVecs; k++)
-                            st_stream(dst + k * (16 / kEB), x[k]);
-                    }
-                } else {
-                    for (int d = 0; d < R; d++) {
-                        E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
-#pragma unroll
-                        for (int k = 0; k < kVecs; k++)
-                            st_stream(dst + k * (16 / kEB), x[k]);
-                    }
-                }
-                continue;
-            }
-            for (int64_t q = e; q < T.len; q++) {
-                E x = src[q];
-                for (int d = 0; d < R; d++)
-                    reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
-            }
-            continue;
-        }
-#pragma unroll
-        for (int k = 0; k < kElemsPerThread; k++) {
-            int64_t q = threadIdx.x + (int64_t)k * kThreads;
-            if (q < T.len) {
-                E x = src[q];
-                for (int d = 0; d < R; d++)
-                    reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
-            }
-        }
-    }
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
+        gather_tile<RC, kEB>(p, R, locate(p.seg, p.nseg, t, false));
 }
 
 // ------------------------------------------- reduce-scatter + AdamW --------
@@ -239,22 +256,18 @@ __device__ __forceinline__ float load_grad(const void *g, int64_t j)
     return __ldcs(reinterpret_cast<const float *>(g) + j);
 }
 
-// Scalar path: rank-ordered fp32 fold of element j, averaged.
-template <bool kGradBf16>
-__device__ __forceinline__ float reduce_scalar(const RsParams &p, int R, int64_t j)
+// Scalar path: rank-ordered fp32 fold of element j, averaged, then AdamW.
+// PP is any parameter block with grad, master, m, v, pshard, gshard, c.
+template <bool kGradBf16, bool kParamBf16, class PP>
+__device__ __forceinline__ void rs_adamw_scalar(const PP &p, int R, const Tile &T, int64_t e)
 {
+    const int r = T.rank;
+    const int64_t j = T.fbase + e;
     float acc = load_grad<kGradBf16>(p.grad[0], j);
     for (int q = 1; q < R; q++)
         acc = __fadd_rn(acc, load_grad<kGradBf16>(p.grad[q], j));
-    return __fmul_rn(acc, p.c.inv_R);
-}
-
-template <bool kGradBf16, bool kParamBf16>
-__device__ __forceinline__ void rs_adamw_scalar(const RsParams &p, int R, const Tile &T, int64_t e)
-{
-    const int r = T.rank;
-    float g = reduce_scalar<kGradBf16>(p, R, T.fbase + e);
-    int64_t s = T.sbase + e;
+    const float g = __fmul_rn(acc, p.c.inv_R);
+    const int64_t s = T.sbase + e;
     AdamOut o = adamw_elem(p.c, g, p.master[r][s], p.m[r][s], p.v[r][s]);
     p.master[r][s] = o.w;
     p.m[r][s] = o.m;
@@ -287,104 +300,109 @@ __device__ __forceinline__ void load_grad8(const void *g, int64_t j, float out[8
     }
 }
 
+// One reduce-scatter + AdamW tile.
+template <int RC, bool kGradBf16, bool kParamBf16, class PP>
+__device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
+{
+    const int r = T.rank;
+    if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
+#pragma unroll 1
+        for (int k = 0; k < kElemsPerThread; k++) {
+            int64_t e = threadIdx.x + (int64_t)k * kThreads;
+            if (e < T.len)
+                rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, e);
+        }
+        return;
+    }
+    const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+    if (e + kElemsPerThread > T.len) {
+        for (int64_t q = e; q < T.len; q++)
+            rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, q);
+        return;
+    }
+    const int64_t j = T.fbase + e;
+    const int64_t s = T.sbase + e;
+    // issue every load of this thread before any arithmetic
+    float acc[8];
+    float4 w0 = ld_f4(p.master[r] + s), w1 = ld_f4(p.master[r] + s + 4);
+    float4 m0 = ld_f4(p.m[r] + s), m1 = ld_f4(p.m[r] + s + 4);
+    float4 v0 = ld_f4(p.v[r] + s), v1 = ld_f4(p.v[r] + s + 4);
+    if (RC > 0 && kGradBf16) {
+        constexpr int kR = RC > 0 ? RC : 1;
+        uint4 raw[kR];
+#pragma unroll
+        for (int q = 0; q < kR; q++)
+            raw[q] = ld_stream(reinterpret_cast<const uint16_t *>(p.grad[q]) + j);
+        unpack_bf16x8(raw[0], acc);
+#pragma unroll
+        for (int q = 1; q < kR; q++) {
+            float g[8];
+            unpack_bf16x8(raw[q], g);
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                acc[k] = __fadd_rn(acc[k], g[k]);
+        }
+    } else if (RC > 0) {
+        constexpr int kR = RC > 0 ? RC : 1;
+        float g[kR][8];
+#pragma unroll
+        for (int q = 0; q < kR; q++)
+            load_grad8<kGradBf16>(p.grad[q], j, g[q]);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            float a = g[0][k];
+#pragma unroll
+            for (int q = 1; q < kR; q++)
+                a = __fadd_rn(a, g[q][k]);
+            acc[k] = a;
+        }
+    } else {
+        load_grad8<kGradBf16>(p.grad[0], j, acc);
+        for (int q = 1; q < R; q++) {
+            float g[8];
+            load_grad8<kGradBf16>(p.grad[q], j, g);
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                acc[k] = __fadd_rn(acc[k], g[k]);
+        }
+    }
+    float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        acc[k] = __fmul_rn(acc[k], p.c.inv_R);
+        AdamOut o = adamw_elem(p.c, acc[k], wv[k], mv[k], vv[k]);
+        wv[k] = o.w;
+        mv[k] = o.m;
+        vv[k] = o.v;
+    }
+    st_f4(p.master[r] + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
+    st_f4(p.master[r] + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
+    st_f4(p.m[r] + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
+    st_f4(p.m[r] + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
+    st_f4(p.v[r] + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    st_f4(p.v[r] + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    if (kParamBf16) {
+        uint4 b;
+        b.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
+        b.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
+        b.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
+        b.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
+        st_stream(p.pshard[r] + s, b);
+    }
+    if (p.gshard[r]) {
+        st_f4(p.gshard[r] + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_f4(p.gshard[r] + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+}
+
 template <int RC, bool kGradBf16, bool kParamBf16>
 __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constant__ RsParams p)
 {
     const int R = RC > 0 ? RC : p.R;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const Tile T = locate(p.seg, p.nseg, t, false);
-        const int r = T.rank;
-        if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
-#pragma unroll 1
-            for (int k = 0; k < kElemsPerThread; k++) {
-                int64_t e = threadIdx.x + (int64_t)k * kThreads;
-                if (e < T.len)
-                    rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, e);
-            }
-            continue;
-        }
-        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
-        if (e + kElemsPerThread > T.len) {
-            for (int64_t q = e; q < T.len; q++)
-                rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, q);
-            continue;
-        }
-        const int64_t j = T.fbase + e;
-        const int64_t s = T.sbase + e;
-        // issue every load of this thread before any arithmetic
-        float acc[8];
-        float4 w0 = ld_f4(p.master[r] + s), w1 = ld_f4(p.master[r] + s + 4);
-        float4 m0 = ld_f4(p.m[r] + s), m1 = ld_f4(p.m[r] + s + 4);
-        float4 v0 = ld_f4(p.v[r] + s), v1 = ld_f4(p.v[r] + s + 4);
-        if (RC > 0 && kGradBf16) {
-            constexpr int kR = RC > 0 ? RC : 1;
-            uint4 raw[kR];
-#pragma unroll
-            for (int q = 0; q < kR; q++)
-                raw[q] = ld_stream(reinterpret_cast<const uint16_t *>(p.grad[q]) + j);
-            unpack_bf16x8(raw[0], acc);
-#pragma unroll
-            for (int q = 1; q < kR; q++) {
-                float g[8];
-                unpack_bf16x8(raw[q], g);
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    acc[k] = __fadd_rn(acc[k], g[k]);
-            }
-        } else if (RC > 0) {
-            constexpr int kR = RC > 0 ? RC : 1;
-            float g[kR][8];
-#pragma unroll
-            for (int q = 0; q < kR; q++)
-                load_grad8<kGradBf16>(p.grad[q], j, g[q]);
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                float a = g[0][k];
-#pragma unroll
-                for (int q = 1; q < kR; q++)
-                    a = __fadd_rn(a, g[q][k]);
-                acc[k] = a;
-            }
-        } else {
-            load_grad8<kGradBf16>(p.grad[0], j, acc);
-            for (int q = 1; q < R; q++) {
-                float g[8];
-                load_grad8<kGradBf16>(p.grad[q], j, g);
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    acc[k] = __fadd_rn(acc[k], g[k]);
-            }
-        }
-        float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            acc[k] = __fmul_rn(acc[k], p.c.inv_R);
-            AdamOut o = adamw_elem(p.c, acc[k], wv[k], mv[k], vv[k]);
-            wv[k] = o.w;
-            mv[k] = o.m;
-            vv[k] = o.v;
-        }
-        st_f4(p.master[r] + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
-        st_f4(p.master[r] + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
-        st_f4(p.m[r] + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
-        st_f4(p.m[r] + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
-        st_f4(p.v[r] + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
-        st_f4(p.v[r] + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
-        if (kParamBf16) {
-            uint4 b;
-            b.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
-            b.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
-            b.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
-            b.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
-            st_stream(p.pshard[r] + s, b);
-        }
-        if (p.gshard[r]) {
-            st_f4(p.gshard[r] + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
-            st_f4(p.gshard[r] + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
-        }
-    }
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
+        rs_adamw_tile<RC, kGradBf16, kParamBf16>(p, R, locate(p.seg, p.nseg, t, false));
 }
 
 // ------------------------------------------------------------ launching ----
@@ -415,8 +433,9 @@ fsdp_status select_device(const void *p, int *dev)
     return FSDP_OK;
 }
 
-// Persistent grid size for `kernel` on `dev`: resident CTAs per SM x SMs.
-fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int *grid)
+// Persistent grid size for `kernel` on `dev`: resident CTAs per SM (at most
+// `max_per_sm`) x SMs.
+fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int max_per_sm, int *grid)
 {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo &d = g_dev[dev];
@@ -433,7 +452,8 @@ fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int *grid)
                              cudaGetErrorString(err));
         it = d.blocks_per_sm.emplace(kernel, nb < 1 ? 1 : nb).first;
     }
-    int64_t g = (int64_t)it->second * d.sms;
+    int per = it->second < max_per_sm ? it->second : max_per_sm;
+    int64_t g = (int64_t)per * d.sms;
     *grid = (int)(tiles < g ? tiles : g);
     return FSDP_OK;
 }
@@ -455,10 +475,12 @@ void fill_segs(Params &p, const LaunchPlan &plan)
 }
 
 template <typename Params, typename Kernel>
-fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const char *what)
+fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const char *what,
+                int max_per_sm)
 {
     int grid = 0;
-    fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), p.total_tiles, &grid);
+    fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), p.total_tiles,
+                              max_per_sm, &grid);
     if (st != FSDP_OK)
         return st;
     kernel<<<grid, kThreads, 0, stream>>>(p);
@@ -485,8 +507,8 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
     for (const LaunchPlan &plan : L->padded_plans) {
         fill_segs(p, plan);
         st = L->param_dtype == FSDP_BF16
-                 ? run(dev, pack_kernel<true>, p, (cudaStream_t)stream, "pack")
-                 : run(dev, pack_kernel<false>, p, (cudaStream_t)stream, "pack");
+                 ? run(dev, pack_kernel<true>, p, (cudaStream_t)stream, "pack", kPackCtasPerSm)
+                 : run(dev, pack_kernel<false>, p, (cudaStream_t)stream, "pack", kPackCtasPerSm);
         if (st != FSDP_OK)
             return st;
     }
@@ -512,15 +534,15 @@ fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
     for (const LaunchPlan &plan : L->valid_plans) {
         fill_segs(p, plan);
         switch (bf16 ? L->R : -L->R) {
-        case 2: st = run(dev, all_gather_kernel<2, 2>, p, s, "all_gather"); break;
-        case 4: st = run(dev, all_gather_kernel<4, 2>, p, s, "all_gather"); break;
-        case 8: st = run(dev, all_gather_kernel<8, 2>, p, s, "all_gather"); break;
-        case -2: st = run(dev, all_gather_kernel<2, 4>, p, s, "all_gather"); break;
-        case -4: st = run(dev, all_gather_kernel<4, 4>, p, s, "all_gather"); break;
-        case -8: st = run(dev, all_gather_kernel<8, 4>, p, s, "all_gather"); break;
+        case 2: st = run(dev, all_gather_kernel<2, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
+        case 4: st = run(dev, all_gather_kernel<4, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
+        case 8: st = run(dev, all_gather_kernel<8, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
+        case -2: st = run(dev, all_gather_kernel<2, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
+        case -4: st = run(dev, all_gather_kernel<4, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
+        case -8: st = run(dev, all_gather_kernel<8, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
         default:
-            st = bf16 ? run(dev, all_gather_kernel<0, 2>, p, s, "all_gather")
-                      : run(dev, all_gather_kernel<0, 4>, p, s, "all_gather");
+            st = bf16 ? run(dev, all_gather_kernel<0, 2>, p, s, "all_gather", kGatherCtasPerSm)
+                      : run(dev, all_gather_kernel<0, 4>, p, s, "all_gather", kGatherCtasPerSm);
         }
         if (st != FSDP_OK)
             return st;
@@ -532,10 +554,10 @@ template <bool kGradBf16, bool kParamBf16>
 static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
 {
     switch (R) {
-    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16>, p, s, "rs_adamw");
-    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16>, p, s, "rs_adamw");
-    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16>, p, s, "rs_adamw");
-    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16>, p, s, "rs_adamw");
+    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
+    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
+    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
+    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
     }
 }
 
@@ -575,6 +597,29 @@ fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, flo
             return st;
     }
     return FSDP_OK;
+}
+
+}  // namespace fsdp
+
+namespace fsdp {
+
+// The reduce-scatter + AdamW of unit A, then the gather of unit B, on one
+// stream. Single launches that interleave the two tile streams (tile by
+// tile, in chunks of 2-32 tiles, or by splitting the CTAs) and two concurrent
+// launches on two streams were all measured on GB300: none beat these two
+// launches back to back (the interleaved forms were 9-17 % slower), so the
+// prefetch is issued in order.
+fsdp_status launch_rs_adamw_gather(const fsdp_layout_t *A, const void *const *grad,
+                                   float *const *master, float *const *m, float *const *v,
+                                   void *const *param_shard_out, float *const *grad_shard_out,
+                                   const AdamScalars &c, const fsdp_layout_t *B,
+                                   const void *const *shard, void *const *full_out, void *stream)
+{
+    fsdp_status st = launch_rs_adamw(A, grad, master, m, v, param_shard_out, grad_shard_out, c,
+                                     stream);
+    if (st != FSDP_OK)
+        return st;
+    return launch_all_gather(B, shard, full_out, stream);
 }
 
 }  // namespace fsdp

@@ -85,3 +85,13 @@ class ShardedUnit:
         self.step = self.step + 1 if step is None else int(step)
         capi.fsdp_reduce_scatter_adamw(self.layout, grads, self.master, self.m, self.v,
                                        self.param_shard, grad_shard_out, hp, self.step, stream)
+
+    def reduce_scatter_adamw_and_gather(self, grads, hp: capi.AdamWHP, other: "ShardedUnit",
+                                        other_full, grad_shard_out=None, step: int | None = None,
+                                        stream=None) -> None:
+        """This unit's optimizer step, then the all-gather of `other` (a different
+        unit, e.g. the next one to be computed), validated together."""
+        self.step = self.step + 1 if step is None else int(step)
+        capi.fsdp_reduce_scatter_adamw_gather(
+            self.layout, grads, self.master, self.m, self.v, self.param_shard, grad_shard_out,
+            hp, self.step, other.layout, other.gather_sources(), other_full, stream)

@@ -160,6 +160,24 @@ fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *layout, const void *c
                                       void *const *param_shard_out, float *const *grad_shard_out,
                                       const fsdp_adamw_hp *hp, int64_t step, void *stream);
 
+/* Prefetch step of two units: the reduce-scatter + AdamW of unit L (the
+ * arguments and results of fsdp_reduce_scatter_adamw) followed on the same
+ * stream by the all-gather + unflatten of unit G (those of
+ * fsdp_all_gather_unflatten) -- the schedule of the pages, which gather the
+ * next unit while the current one's gradients are reduced ("FSDP2 的参数全
+ * 聚合、梯度归约分片与显存峰值", §07 forward prefetch; "从源码理解 FSDP", §5.2
+ * layer-wise all-gather overlap). Both operations are validated together:
+ * every buffer of one must be disjoint from every output of the other (so G
+ * may not be the unit being updated), which leaves the library free to order
+ * or overlap them. On GB300 the two launches back to back were faster than
+ * any single launch interleaving them, so that is what is issued.
+ * Errors as for the two calls. */
+fsdp_status fsdp_reduce_scatter_adamw_gather(
+    const fsdp_layout_t *L, const void *const *grad_full, float *const *master, float *const *m,
+    float *const *v, void *const *param_shard_out, float *const *grad_shard_out,
+    const fsdp_adamw_hp *hp, int64_t step, const fsdp_layout_t *G, const void *const *shard,
+    void *const *full_out, void *stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 const char *fsdp_last_error(void);
 

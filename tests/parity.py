@@ -172,3 +172,42 @@ def run_unit_case(case: UnitCase, w=None, grads=None, moments=None):
             assert_master_close(got, want_full[d], f"gather after step full[{d}]")
     torch.cuda.synchronize()
     return {"P": U.P, "exact_master_fraction": exact_master / max(1, case.R * U.S)}
+
+
+def run_overlap_case(case_rs: UnitCase, case_ag: UnitCase, seed_shift: int = 500):
+    """The prefetch call: reduce-scatter + AdamW of one unit and all-gather
+    of another, each compared with the oracle."""
+    w_a, grads = host_inputs(case_rs)
+    case_b = UnitCase(**{**case_ag.__dict__, "seed": case_ag.seed + seed_shift})
+    w_b, _ = host_inputs(case_b)
+    mk = lambda c: (oracle.layout(oracle.FLAT if c.mode == "flat" else oracle.PER_PARAM, c.R,
+                                  c.shapes),
+                    ShardedUnit(c.shapes, c.R, c.mode, c.param_dtype, c.grad_dtype))
+    Oa, Ua = mk(case_rs)
+    Ob, Ub = mk(case_b)
+    bf_a, bf_b = case_rs.param_dtype == "bf16", case_b.param_dtype == "bf16"
+    Ua.shard_from_full(to_dev(w_a))
+    Ub.shard_from_full(to_dev(w_b))
+    masters_a, _ = oracle.pack(Oa, w_a, with_bf16=bf_a)
+    masters_b, p16_b = oracle.pack(Ob, w_b, with_bf16=bf_b)
+    m = [np.zeros(Ua.S, np.float32) for _ in range(case_rs.R)]
+    v = [np.zeros(Ua.S, np.float32) for _ in range(case_rs.R)]
+    lr, b1, b2, eps, wd = case_rs.hp
+    full_b = Ub.alloc_full()
+    gsh = [torch.zeros(Ua.S, dtype=torch.float32, device="cuda") for _ in range(case_rs.R)]
+    Ua.reduce_scatter_adamw_and_gather([to_dev(g) for g in grads], AdamWHP(lr, b1, b2, eps, wd),
+                                       Ub, full_b, grad_shard_out=gsh, step=case_rs.step)
+    want_g, want_p16 = oracle.rs_adamw(Oa, grads, masters_a, m, v,
+                                       oracle.AdamWHP(lr, b1, b2, eps, wd), case_rs.step,
+                                       with_bf16=bf_a)
+    want_full = oracle.all_gather(Ob, p16_b if bf_b else masters_b)
+    for d in range(case_b.R):
+        assert_bits_equal(host(full_b[d]), want_full[d], f"overlapped gather full[{d}]")
+    for r in range(case_rs.R):
+        assert_bits_equal(host(gsh[r]), want_g[r], f"overlapped reduce-scatter shard[{r}]")
+        assert_master_close(host(Ua.master[r]), masters_a[r], f"overlapped master[{r}]")
+        assert_moment_close(host(Ua.m[r]), m[r], f"overlapped m[{r}]")
+        assert_moment_close(host(Ua.v[r]), v[r], f"overlapped v[{r}]")
+        if bf_a:
+            assert_bf16_close(host(Ua.param_shard[r]), want_p16[r], f"overlapped bf16[{r}]")
+    torch.cuda.synchronize()

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from fully_sharded_state_gb300 import synth
-from parity import UnitCase, run_unit_case
+from parity import UnitCase, run_overlap_case, run_unit_case
 
 pytestmark = pytest.mark.gpu
 
@@ -140,3 +140,33 @@ def test_device_errors_launch_nothing(cuda_lib):
 def test_native_library_is_loaded(cuda_lib):
     maps = open("/proc/self/maps").read()
     assert "libfsdp_shard.so" in maps
+
+
+OVERLAP = {
+    "block_and_block": (EDGE["odd_width_bf16"], UnitCase([(512,), (512, 512), (2048, 512)], R=4)),
+    "ragged_fp32_pair": (UnitCase([(1001, 3), (7, 513), (1, 64)], R=8, param_dtype="f32",
+                                  grad_dtype="f32", g_std=1.0, w_std=1.0, outlier_frac=0.01),
+                         UnitCase([(127, 513), (3, 1), (4097, 1)], R=8, param_dtype="f32",
+                                  grad_dtype="f32")),
+    "flat_rs_per_param_gather": (UnitCase([(1001, 3), (5, 7)], R=4, mode="flat"),
+                                 UnitCase([(300, 70)], R=4)),
+    "generic_R5": (UnitCase([(513, 64), (9,)], R=5), UnitCase([(77, 40)], R=5)),
+    "tiny_rs_big_gather": (UnitCase([(3,)], R=2), UnitCase([(4096, 64)], R=2)),
+    "different_R": (UnitCase([(256, 40)], R=4), UnitCase([(256, 40)], R=8)),
+    "different_dtype": (UnitCase([(256, 40)], R=4), UnitCase([(256, 40)], R=4,
+                                                            param_dtype="f32")),
+    "many_params": (EDGE["many_params_several_launches"], UnitCase([(64, 8)], R=8)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(OVERLAP))
+def test_prefetch_reduce_scatter_then_gather(cuda_lib, name):
+    run_overlap_case(*OVERLAP[name])
+
+
+def test_prefetch_rejects_gathering_the_updated_unit(cuda_lib):
+    from fully_sharded_state_gb300 import AdamWHP, FsdpError, ShardedUnit
+    U = ShardedUnit([(64, 64)], R=2)
+    with pytest.raises(FsdpError):
+        U.reduce_scatter_adamw_and_gather(U.alloc_grads(), AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01),
+                                          U, U.alloc_full())
