@@ -81,6 +81,9 @@ def _load(path: str):
     L.orc_owner.restype = ctypes.c_int
     L.orc_owner.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
                             ctypes.c_int64, _i64p, _i64p, _i64p]
+    L.orc_all_reduce.restype = None
+    L.orc_all_reduce.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vpp,
+                                 ctypes.c_int, _vpp]
     L.orc_rs_adamw.restype = ctypes.c_int
     L.orc_rs_adamw.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
                                ctypes.c_int, _vpp, _vpp, _vpp, _vpp, _vpp, _vpp,
@@ -281,3 +284,15 @@ def owner(L: Layout, js) -> tuple:
     if rc != 0:
         raise ValueError("oracle: element index outside the unit")
     return rank, index
+
+
+def all_reduce(grads, out_bf16: bool) -> list:
+    """DDP all-reduce: R identical full outputs of the fixed-order average
+    (float32, or bf16 bits as uint16)."""
+    grads = [np.ascontiguousarray(g) for g in grads]
+    R, P = len(grads), grads[0].size
+    dt = np.uint16 if out_bf16 else np.float32
+    out = [np.zeros(P, dt) for _ in range(R)]
+    lib().orc_all_reduce(R, P, _gdtype(grads[0]), _ptrs(grads), BF16 if out_bf16 else F32,
+                         _ptrs(out))
+    return out

@@ -396,3 +396,31 @@ int orc_owner(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* All-reduce (DDP): every rank receives the average over ranks of all  */
+/* R full local gradients ([Walkthrough] DDP comparison; [FSDP2] §09:   */
+/* DDP all-reduce leaves every card the full averaged gradient; the     */
+/* reduce-scatter gives rank r only segment r of the same result).      */
+/* grad[q]: rank q's P gradient values (grad_dtype); out[d]: rank d's    */
+/* P outputs in out_dtype (fp32, or bf16 RNE of the fp32 average).      */
+/* Same per-element fold as orc_sum_ranks.                              */
+/* ------------------------------------------------------------------ */
+void orc_all_reduce(int64_t R, int64_t P, int grad_dtype, const void *const *grad,
+                    int out_dtype, void *const *out)
+{
+    int64_t esize = grad_dtype == ORC_BF16 ? 2 : 4;
+    const void *ptrs[R];
+    float avg[1];
+    for (int64_t j = 0; j < P; j++) {
+        for (int64_t q = 0; q < R; q++)
+            ptrs[q] = (const char *)grad[q] + j * esize;
+        orc_sum_ranks(R, 1, grad_dtype, ptrs, avg);
+        for (int64_t d = 0; d < R; d++) {
+            if (out_dtype == ORC_BF16)
+                ((uint16_t *)out[d])[j] = orc_f32_to_bf16(avg[0]);
+            else
+                ((float *)out[d])[j] = avg[0];
+        }
+    }
+}

@@ -400,6 +400,39 @@ def check_reduce_scatter_is_allreduce_then_slice():
                 assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
+def check_all_reduce_is_gather_of_reduce_scatter():
+    """All-reduce == all-gather of the reduce-scatter shards, bit for bit, in
+    both layouts ("FSDP2 的参数全聚合、梯度归约分片与显存峰值", §09; "从源码理解
+    FSDP", §2.3: reduce-scatter equals all-reduce followed by taking segment
+    r); and with integer gradients the all-reduce is the exact average."""
+    rng = np.random.default_rng(23)
+    for trial in range(40):
+        shapes = _tiny_shapes(rng)
+        R = int(rng.integers(1, 9))
+        P = sum(int(np.prod(s)) for s in shapes)
+        gf = [rng.standard_normal(P).astype(np.float32) for _ in range(R)]
+        for gdt in ("f32", "bf16"):
+            grads = gf if gdt == "f32" else [oracle.f32_to_bf16(x) for x in gf]
+            ar = oracle.all_reduce(grads, out_bf16=False)
+            for d in range(1, R):
+                assert np.array_equal(ar[d].view(np.uint32), ar[0].view(np.uint32))
+            ar16 = oracle.all_reduce(grads, out_bf16=True)
+            assert np.array_equal(ar16[R - 1], oracle.f32_to_bf16(ar[0]))
+            for mode in (oracle.PER_PARAM, oracle.FLAT):
+                L = oracle.layout(mode, R, shapes)
+                gathered = oracle.all_gather(L, oracle.reduce_scatter(L, grads))
+                for d in range(R):
+                    assert np.array_equal(gathered[d].view(np.uint32), ar[0].view(np.uint32))
+        gi = [rng.integers(-64, 65, P) for _ in range(R)]
+        ar = oracle.all_reduce([x.astype(np.float32) for x in gi], out_bf16=False)
+        for j in range(P):
+            exact = Fraction(int(sum(int(x[j]) for x in gi)), R)
+            if R in (1, 2, 4, 8):
+                assert Fraction(float(ar[0][j])) == exact
+            else:
+                assert abs(Fraction(float(ar[0][j])) - exact) <= abs(exact) * Fraction(1, 2 ** 22)
+
+
 def check_reduce_scatter_special_cases():
     # R = 1: the shard is the gradient itself
     g = np.array([1.5, -2.25, 3e-8, -0.0], np.float32)

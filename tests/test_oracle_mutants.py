@@ -77,12 +77,20 @@ MUTANTS = [
      "index[k] = shard_off[i] + (e - full_off[i]);"),
     ("flat owner uses the unpadded size",
      "rank[k] = e / S;", "rank[k] = e / (P / R > 0 ? P / R : 1); if (rank[k] >= R) rank[k] = R - 1;"),
+    ("all-reduce writes only rank 0's output",
+     "        for (int64_t d = 0; d < R; d++) {\n            if (out_dtype == ORC_BF16)",
+     "        for (int64_t d = 0; d < 1; d++) {\n            if (out_dtype == ORC_BF16)"),
+    ("all-reduce reads one element off",
+     "ptrs[q] = (const char *)grad[q] + j * esize;\n        orc_sum_ranks",
+     "ptrs[q] = (const char *)grad[q] + (j + 1 < P ? j + 1 : j) * esize;\n        orc_sum_ranks"),
     ("bf16 widening takes the low half",
      "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h;"),
 ]
 
+# A mutant may write out of bounds inside its own child process, so the child
+# leaves with os._exit as soon as a pin fails, before any interpreter teardown.
 _RUNNER = r"""
-import sys
+import os, sys
 sys.path[:0] = [{repo!r}, {tests!r}]
 import oracle
 oracle.use_library({lib!r})
@@ -91,8 +99,8 @@ for check in pins.ALL_CHECKS:
     try:
         check()
     except Exception as exc:  # a pin that fails or errors out on the mutant
-        print("caught by", check.__name__, type(exc).__name__)
-        sys.exit(3)
+        print("caught by", check.__name__, type(exc).__name__, flush=True)
+        os._exit(3)
 print("not caught")
 sys.exit(0)
 """
