@@ -360,6 +360,30 @@ def run_ours(args):
                    "avg_launch_ms": round(ag_avg_ms, 4),
                    "traffic": profiled_traffic("all_gather", args.workload)}
 
+    # DDP's collective on the same unit, for comparison: all-reduce of the R
+    # bf16 gradients into R fp32 full outputs (reduce dtype fp32)
+    U0 = units[0]
+    ar_out = [torch.empty(U0.P, dtype=torch.float32, device=dev) for _ in range(R)]
+    for _ in range(3):
+        U0.all_reduce(grads[0], ar_out, "f32", stream=stream)
+    ar_ms = []
+    for _ in range(20):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        U0.all_reduce(grads[0], ar_out, "f32", stream=stream)
+        b.record(stream)
+        b.synchronize()
+        ar_ms.append(a.elapsed_time(b))
+    del ar_out
+    ar_bytes = R * U0.P * (2 + 4)
+    ar_avg = statistics.mean(ar_ms)
+    peak, peak_src = measured_peak()
+    ddp = {"kernel": "all_reduce_kernel (DDP all-reduce: bf16 grads -> fp32 outputs)",
+           "bound": "hbm", "achieved": round(ar_bytes / (ar_avg * 1e-3) / 1e9, 1), "peak": peak,
+           "unit": "GB/s", "frac": round(ar_bytes / (ar_avg * 1e-3) / 1e9 / peak, 4),
+           "algorithmic_bytes_per_launch": ar_bytes, "avg_launch_ms": round(ar_avg, 4),
+           "traffic": profiled_traffic("all_reduce", args.workload)}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes)
@@ -380,7 +404,7 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (>= 3.9 GB streamed per launch); no flush",
                            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 "pct_of_hbm_peak": round(value / world / peak, 4),
-                "roofline": roofline, "roofline_all_gather": roofline_ag,
+                "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
                 "clocks": clocks.summary(), "gpu_launches": launches,
                 "cpu_baseline": cpu, "e2e": e2e}
         print(json.dumps(line), flush=True)

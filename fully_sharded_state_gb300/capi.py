@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH):
         _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
         ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(AdamWHP), ctypes.c_int64,
         _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp]
+    L.fsdp_all_reduce.restype = ctypes.c_int
+    L.fsdp_all_reduce.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int, _vp]
     L.fsdp_last_error.restype = ctypes.c_char_p
     L.fsdp_last_error.argtypes = []
     L.fsdp_version.restype = ctypes.c_char_p
@@ -232,6 +234,14 @@ def fsdp_reduce_scatter_adamw_gather(layout: Layout, grad_full, master, m, v, pa
         _ptr_array(grad_shard_out, R, "grad_shard_out", allow_none=True),
         ctypes.byref(hp), int(step), gather_layout.handle, _ptr_array(shard, G, "shard"),
         _ptr_array(full_out, G, "full_out"), _stream_handle(stream)))
+
+
+def fsdp_all_reduce(layout: Layout, grad_full, out, out_dtype: int, stream=None) -> None:
+    """DDP all-reduce: every rank's output gets the fixed-order average."""
+    R = layout.R
+    _check(load().fsdp_all_reduce(layout.handle, _ptr_array(grad_full, R, "grad_full"),
+                                  _ptr_array(out, R, "out"), int(out_dtype),
+                                  _stream_handle(stream)))
 
 
 def fsdp_version() -> str:

@@ -448,4 +448,26 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
                                   adam_scalars(hp, step, L->R), G, shard, full_out, stream);
 }
 
+fsdp_status fsdp_all_reduce(const fsdp_layout_t *L, const void *const *grad_full,
+                            void *const *out, fsdp_dtype out_dtype, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_all_reduce: layout is NULL");
+    if (out_dtype != FSDP_F32 && out_dtype != FSDP_BF16)
+        return set_error(FSDP_EUNSUPPORTED, "fsdp_all_reduce: unsupported output dtype");
+    if (L->P == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    fsdp_status st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
+                                &spans);
+    if (st == FSDP_OK)
+        st = check_ptrs((const void *const *)out, L->R, L->P * esize(out_dtype), true, "out",
+                        &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
+        return st;
+    return launch_all_reduce(L, grad_full, out, out_dtype, stream);
+}
+
 }  // extern "C"

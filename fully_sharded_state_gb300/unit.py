@@ -95,3 +95,8 @@ class ShardedUnit:
         capi.fsdp_reduce_scatter_adamw_gather(
             self.layout, grads, self.master, self.m, self.v, self.param_shard, grad_shard_out,
             hp, self.step, other.layout, other.gather_sources(), other_full, stream)
+
+    def all_reduce(self, grads, out, out_dtype: str = "f32", stream=None) -> None:
+        """DDP's all-reduce of the R full gradients into R full outputs
+        (fp32 or bf16), for comparison with the sharded path."""
+        capi.fsdp_all_reduce(self.layout, grads, out, _DT[out_dtype][0], stream)

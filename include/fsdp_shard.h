@@ -178,6 +178,19 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
     const fsdp_adamw_hp *hp, int64_t step, const fsdp_layout_t *G, const void *const *shard,
     void *const *full_out, void *stream);
 
+/* All-reduce, the DDP collective that FSDP is compared against ("FSDP
+ * Training Step Walkthrough", per-step communication summary; "FSDP2 的参数
+ * 全聚合、梯度归约分片与显存峰值", §01 and §09). Every rank d receives, for
+ * every unit element j, the same fixed-order average as the reduce-scatter:
+ *   acc = g_0[j] + g_1[j] + ... + g_{R-1}[j] (fp32, left to right);
+ *   out[d][j] = acc * fl(1/R), stored as fp32 or as its bf16 rounding.
+ * So gathering the fp32 reduce-scatter shards reproduces out[d] bit for bit.
+ * grad_full[q]: rank q's P elements of the layout's grad_dtype; out[d]: P
+ * elements of out_dtype. Only R, P and the grad dtype of the layout are
+ * used. Errors: FSDP_EINVAL, FSDP_EALIGN, FSDP_EUNSUPPORTED (out_dtype). */
+fsdp_status fsdp_all_reduce(const fsdp_layout_t *layout, const void *const *grad_full,
+                            void *const *out, fsdp_dtype out_dtype, void *stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 const char *fsdp_last_error(void);
 

@@ -241,3 +241,18 @@ def test_binding_rejects_host_tensors(lib):
     t = [torch.zeros(8), torch.zeros(8)]
     with pytest.raises(ValueError):
         capi.fsdp_all_gather_unflatten(L, t, t)
+
+
+def test_all_reduce_rejects_bad_arguments(lib):
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(4096, 16)], capi.FSDP_BF16, capi.FSDP_BF16)
+    MB = 1 << 20
+    g = _ptrs([BASE, BASE + MB])
+    assert lib.fsdp_all_reduce(L.handle, g, _ptrs([BASE + 4 * MB, BASE + 8 * MB]), 7,
+                               None) == capi.FSDP_EUNSUPPORTED
+    # an output overlapping a gradient
+    assert lib.fsdp_all_reduce(L.handle, g, _ptrs([BASE + 64, BASE + 8 * MB]), capi.FSDP_F32,
+                               None) == capi.FSDP_EINVAL
+    # fp32 outputs of 256 KB each overlap when placed 128 KB apart
+    assert lib.fsdp_all_reduce(L.handle, g, _ptrs([BASE + 4 * MB, BASE + 4 * MB + (1 << 17)]),
+                               capi.FSDP_F32, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_all_reduce(None, g, g, capi.FSDP_F32, None) == capi.FSDP_EINVAL

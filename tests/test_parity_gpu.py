@@ -170,3 +170,51 @@ def test_prefetch_rejects_gathering_the_updated_unit(cuda_lib):
     with pytest.raises(FsdpError):
         U.reduce_scatter_adamw_and_gather(U.alloc_grads(), AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01),
                                           U, U.alloc_full())
+
+
+ALL_REDUCE = {
+    "block_bf16_to_f32": (UnitCase([(512,), (512, 512), (2048, 512)], R=4), "f32"),
+    "bf16_to_bf16_R8": (UnitCase([(4097, 8), (3,)], R=8, seed=31), "bf16"),
+    "f32_R3_outliers": (UnitCase([(1001, 5)], R=3, grad_dtype="f32", param_dtype="f32",
+                                 g_std=1.0, outlier_frac=0.01, seed=32), "f32"),
+    "R1_copy": (UnitCase([(77, 13)], R=1, seed=33), "f32"),
+    "ragged_tail_generic_R6": (UnitCase([(2049, 3), (5,)], R=6, seed=34), "bf16"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ALL_REDUCE))
+def test_all_reduce(cuda_lib, name):
+    import oracle
+    from fully_sharded_state_gb300 import ShardedUnit
+    from parity import assert_bits_equal, host, host_inputs, to_dev
+    case, out_dt = ALL_REDUCE[name]
+    _, grads = host_inputs(case)
+    U = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype)
+    tdt = torch.bfloat16 if out_dt == "bf16" else torch.float32
+    out = [torch.zeros(U.P, dtype=tdt, device="cuda") for _ in range(case.R)]
+    U.all_reduce([to_dev(g) for g in grads], out, out_dt)
+    want = oracle.all_reduce(grads, out_bf16=out_dt == "bf16")
+    for d in range(case.R):
+        assert_bits_equal(host(out[d]), want[d], f"all-reduce out[{d}]")
+
+
+@pytest.mark.parametrize("mode", ["per_param", "flat"])
+def test_all_reduce_equals_gather_of_reduce_scatter(cuda_lib, mode):
+    """On the GPU: gathering the fp32 reduce-scatter shards gives the
+    all-reduce output bit for bit."""
+    from fully_sharded_state_gb300 import AdamWHP, ShardedUnit
+    from parity import host_inputs, to_dev
+    case = UnitCase([(1001, 3), (257, 64), (9,)], R=4, mode=mode, seed=35)
+    _, grads = host_inputs(case)
+    g = [to_dev(x) for x in grads]
+    U = ShardedUnit(case.shapes, 4, mode, "bf16", "bf16")
+    gsh = [torch.zeros(U.S, dtype=torch.float32, device="cuda") for _ in range(4)]
+    U.reduce_scatter_adamw(g, AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01), grad_shard_out=gsh)
+    F = ShardedUnit(case.shapes, 4, mode, "f32", "bf16")   # same layout, fp32 shards
+    gathered = F.alloc_full()
+    from fully_sharded_state_gb300 import capi
+    capi.fsdp_all_gather_unflatten(F.layout, gsh, gathered)
+    out = [torch.empty(U.P, dtype=torch.float32, device="cuda") for _ in range(4)]
+    U.all_reduce(g, out, "f32")
+    for d in range(4):
+        assert torch.equal(gathered[d].view(torch.int32), out[d].view(torch.int32))
