@@ -84,6 +84,9 @@ def _load(path: str):
     L.orc_all_reduce.restype = None
     L.orc_all_reduce.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vpp,
                                  ctypes.c_int, _vpp]
+    L.orc_accumulate.restype = None
+    L.orc_accumulate.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vpp, _vpp,
+                                 ctypes.c_int]
     L.orc_rs_adamw.restype = ctypes.c_int
     L.orc_rs_adamw.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
                                ctypes.c_int, _vpp, _vpp, _vpp, _vpp, _vpp, _vpp,
@@ -296,3 +299,12 @@ def all_reduce(grads, out_bf16: bool) -> list:
     lib().orc_all_reduce(R, P, _gdtype(grads[0]), _ptrs(grads), BF16 if out_bf16 else F32,
                          _ptrs(out))
     return out
+
+
+def accumulate(acc, grads, first: bool) -> None:
+    """In place: acc[q] = g[q] (first micro-batch) or acc[q] + g[q], fp32."""
+    grads = [np.ascontiguousarray(g) for g in grads]
+    for a in acc:
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    lib().orc_accumulate(len(grads), grads[0].size, _gdtype(grads[0]), _ptrs(acc),
+                         _ptrs(grads), int(bool(first)))

@@ -424,3 +424,26 @@ void orc_all_reduce(int64_t R, int64_t P, int grad_dtype, const void *const *gra
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Gradient accumulation over micro-batches ([FSDP2] §08: each micro-   */
+/* batch runs forward/backward; the update happens once per K micro-    */
+/* batches). For every rank q and element j, in micro-batch order:      */
+/*   first micro-batch: acc[q][j] = g[q][j]        (exact widening)     */
+/*   later ones:        acc[q][j] = acc[q][j] + g[q][j]   (fp32)        */
+/* The accumulated gradient is the plain sum over micro-batches; the     */
+/* reduce-scatter of the accumulators then averages over ranks.          */
+/* ------------------------------------------------------------------ */
+void orc_accumulate(int64_t R, int64_t P, int grad_dtype, float *const *acc,
+                    const void *const *grad, int first)
+{
+    for (int64_t q = 0; q < R; q++) {
+        for (int64_t j = 0; j < P; j++) {
+            float g = load_as_f32(grad[q], grad_dtype, j);
+            if (first)
+                acc[q][j] = g;
+            else
+                acc[q][j] = acc[q][j] + g;
+        }
+    }
+}

@@ -433,6 +433,53 @@ def check_all_reduce_is_gather_of_reduce_scatter():
                 assert abs(Fraction(float(ar[0][j])) - exact) <= abs(exact) * Fraction(1, 2 ** 22)
 
 
+def check_accumulation_is_the_micro_batch_sum():
+    """K micro-batches of integer gradients accumulate to their exact sum;
+    the reduce-scatter of the accumulators equals the brute-force sum over
+    micro-batches and ranks divided by R; the first micro-batch is copied,
+    not added to zero, so -0 survives; accumulation is in micro-batch order
+    (checked with values where the order changes the fp32 result)."""
+    rng = np.random.default_rng(29)
+    for trial in range(20):
+        shapes = _tiny_shapes(rng)
+        R = int(rng.integers(1, 6))
+        K = int(rng.integers(1, 5))
+        P = sum(int(np.prod(s)) for s in shapes)
+        micro = [[rng.integers(-60, 61, P) for _ in range(R)] for _ in range(K)]
+        for gdt in ("f32", "bf16"):
+            acc = [np.zeros(P, np.float32) for _ in range(R)]
+            for k in range(K):
+                gk = [x.astype(np.float32) for x in micro[k]]
+                if gdt == "bf16":
+                    gk = [oracle.f32_to_bf16(x) for x in gk]
+                oracle.accumulate(acc, gk, first=(k == 0))
+            for q in range(R):
+                want = sum(micro[k][q] for k in range(K))
+                assert np.array_equal(acc[q], want.astype(np.float32))
+            L = oracle.layout(oracle.PER_PARAM, R, shapes)
+            gsh = oracle.reduce_scatter(L, acc)
+            ranges = brute.per_param_owner_ranges(shapes, R)
+            tot = [[int(sum(micro[k][q][j] for k in range(K))) for j in range(P)] for q in range(R)]
+            sums = brute.reduce_scatter_sum(tot, R, ranges)
+            for r in range(R):
+                got = np.concatenate([_owned(L, r, i, gsh[r]) for i in range(len(shapes))])
+                for x, sm in zip(got.tolist(), sums[r]):
+                    exact = Fraction(sm, R)
+                    if R in (1, 2, 4):
+                        assert Fraction(x) == exact
+                    else:
+                        assert abs(Fraction(x) - exact) <= abs(exact) * Fraction(1, 2 ** 22)
+    acc = [np.zeros(2, np.float32)]
+    oracle.accumulate(acc, [np.array([-0.0, 5.0], np.float32)], first=True)
+    assert np.signbit(acc[0][0]) and acc[0][1] == 5.0
+    # (1 + 2^-24) + 2^-24 rounds differently from 1 + (2^-24 + 2^-24)
+    e = np.float32(2.0 ** -24)
+    acc = [np.zeros(1, np.float32)]
+    for k, x in enumerate([np.float32(1.0), e, e]):
+        oracle.accumulate(acc, [np.array([x], np.float32)], first=(k == 0))
+    assert acc[0][0] == (np.float32(1.0) + e) + e
+
+
 def check_reduce_scatter_special_cases():
     # R = 1: the shard is the gradient itself
     g = np.array([1.5, -2.25, 3e-8, -0.0], np.float32)

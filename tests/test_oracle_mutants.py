@@ -83,6 +83,11 @@ MUTANTS = [
     ("all-reduce reads one element off",
      "ptrs[q] = (const char *)grad[q] + j * esize;\n        orc_sum_ranks",
      "ptrs[q] = (const char *)grad[q] + (j + 1 < P ? j + 1 : j) * esize;\n        orc_sum_ranks"),
+    ("accumulation ignores the first flag",
+     "            if (first)\n                acc[q][j] = g;",
+     "            if (0)\n                acc[q][j] = g;"),
+    ("accumulation overwrites instead of adding",
+     "                acc[q][j] = acc[q][j] + g;", "                acc[q][j] = g;"),
     ("bf16 widening takes the low half",
      "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h;"),
 ]
