@@ -384,6 +384,46 @@ def run_ours(args):
            "algorithmic_bytes_per_launch": ar_bytes, "avg_launch_ms": round(ar_avg, 4),
            "traffic": profiled_traffic("all_reduce", args.workload)}
 
+    # gradient accumulation on the same unit: one more micro-batch added into
+    # the fp32 accumulators, and the last micro-batch fused into the step
+    acc = U0.alloc_accumulators()
+    U0.accumulate_grad(grads[0], acc, first=True, stream=stream)
+
+    def timed_launches(fn, n=20):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.mean(ms)
+
+    acc_ms = timed_launches(lambda: U0.accumulate_grad(grads[0], acc, first=False, stream=stream))
+    rsacc_ms = timed_launches(lambda: U0.reduce_scatter_adamw_accum(acc, grads[0], hp,
+                                                                     stream=stream))
+    del acc
+    acc_bytes = R * U0.P * (4 + 2 + 4)
+    rsacc_bytes = U0.P * (R * (4 + 2) + 24 + 2)
+    gbs = lambda nb, ms: round(nb / (ms * 1e-3) / 1e9, 1)
+    accumulation = {
+        "accumulate": {"kernel": "accumulate_kernel (acc += bf16 micro-batch grads, R ranks)",
+                       "achieved": gbs(acc_bytes, acc_ms), "frac": round(gbs(acc_bytes, acc_ms)
+                                                                         / peak, 4),
+                       "unit": "GB/s", "algorithmic_bytes_per_launch": acc_bytes,
+                       "avg_launch_ms": round(acc_ms, 4),
+                       "traffic": profiled_traffic("accumulate", args.workload)},
+        "rs_adamw_accum": {"kernel": "rs_adamw_kernel with accumulators (last micro-batch "
+                                     "fused into reduce-scatter + AdamW)",
+                           "achieved": gbs(rsacc_bytes, rsacc_ms),
+                           "frac": round(gbs(rsacc_bytes, rsacc_ms) / peak, 4), "unit": "GB/s",
+                           "algorithmic_bytes_per_launch": rsacc_bytes,
+                           "avg_launch_ms": round(rsacc_ms, 4),
+                           "traffic": profiled_traffic("rs_adamw_accum", args.workload)}}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes)
@@ -405,6 +445,7 @@ def run_ours(args):
                            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 "pct_of_hbm_peak": round(value / world / peak, 4),
                 "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
+                "grad_accumulation": accumulation,
                 "clocks": clocks.summary(), "gpu_launches": launches,
                 "cpu_baseline": cpu, "e2e": e2e}
         print(json.dumps(line), flush=True)

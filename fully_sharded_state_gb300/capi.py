@@ -82,6 +82,14 @@ def load(path: str = LIB_PATH):
         _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp]
     L.fsdp_all_reduce.restype = ctypes.c_int
     L.fsdp_all_reduce.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int, _vp]
+    L.fsdp_accumulate_grad.restype = ctypes.c_int
+    L.fsdp_accumulate_grad.argtypes = [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int,
+                                       _vp]
+    L.fsdp_reduce_scatter_adamw_accum.restype = ctypes.c_int
+    L.fsdp_reduce_scatter_adamw_accum.argtypes = [
+        _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+        ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(AdamWHP),
+        ctypes.c_int64, _vp]
     L.fsdp_last_error.restype = ctypes.c_char_p
     L.fsdp_last_error.argtypes = []
     L.fsdp_version.restype = ctypes.c_char_p
@@ -242,6 +250,27 @@ def fsdp_all_reduce(layout: Layout, grad_full, out, out_dtype: int, stream=None)
     _check(load().fsdp_all_reduce(layout.handle, _ptr_array(grad_full, R, "grad_full"),
                                   _ptr_array(out, R, "out"), int(out_dtype),
                                   _stream_handle(stream)))
+
+
+def fsdp_accumulate_grad(layout: Layout, acc_full, grad_full, first: bool, stream=None) -> None:
+    """Add one micro-batch's gradients into the R fp32 accumulators (copy if first)."""
+    R = layout.R
+    _check(load().fsdp_accumulate_grad(layout.handle, _ptr_array(acc_full, R, "acc_full"),
+                                       _ptr_array(grad_full, R, "grad_full"), int(bool(first)),
+                                       _stream_handle(stream)))
+
+
+def fsdp_reduce_scatter_adamw_accum(layout: Layout, acc_full, grad_full, master, m, v,
+                                    param_shard_out, grad_shard_out, hp: AdamWHP, step: int,
+                                    stream=None) -> None:
+    """The last micro-batch fused into reduce-scatter + AdamW."""
+    R = layout.R
+    _check(load().fsdp_reduce_scatter_adamw_accum(
+        layout.handle, _ptr_array(acc_full, R, "acc_full"), _ptr_array(grad_full, R, "grad_full"),
+        _ptr_array(master, R, "master"), _ptr_array(m, R, "m"), _ptr_array(v, R, "v"),
+        _ptr_array(param_shard_out, R, "param_shard_out", allow_none=True),
+        _ptr_array(grad_shard_out, R, "grad_shard_out", allow_none=True),
+        ctypes.byref(hp), int(step), _stream_handle(stream)))
 
 
 def fsdp_version() -> str:

@@ -470,4 +470,47 @@ fsdp_status fsdp_all_reduce(const fsdp_layout_t *L, const void *const *grad_full
     return launch_all_reduce(L, grad_full, out, out_dtype, stream);
 }
 
+fsdp_status fsdp_accumulate_grad(const fsdp_layout_t *L, float *const *acc_full,
+                                 const void *const *grad_full, int first, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_accumulate_grad: layout is NULL");
+    if (L->P == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    fsdp_status st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
+                                &spans);
+    if (st == FSDP_OK)
+        st = check_ptrs((const void *const *)acc_full, L->R, L->P * 4, true, "acc_full", &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
+        return st;
+    return launch_accumulate(L, acc_full, grad_full, first, stream);
+}
+
+fsdp_status fsdp_reduce_scatter_adamw_accum(const fsdp_layout_t *L, const float *const *acc_full,
+                                            const void *const *grad_full, float *const *master,
+                                            float *const *m, float *const *v,
+                                            void *const *param_shard_out,
+                                            float *const *grad_shard_out, const fsdp_adamw_hp *hp,
+                                            int64_t step, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_reduce_scatter_adamw_accum: layout is NULL");
+    fsdp_status st = check_hp(hp, step);
+    if (st != FSDP_OK || L->P == 0)
+        return st;
+    std::vector<Span> spans;
+    st = check_ptrs((const void *const *)acc_full, L->R, L->P * 4, false, "acc_full", &spans);
+    if (st == FSDP_OK)
+        st = check_rs_args(L, grad_full, master, m, v, param_shard_out, grad_shard_out, &spans);
+    if (st == FSDP_OK)
+        st = check_overlap(spans);
+    if (st != FSDP_OK)
+        return st;
+    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                           adam_scalars(hp, step, L->R), stream, acc_full);
+}
+
 }  // extern "C"

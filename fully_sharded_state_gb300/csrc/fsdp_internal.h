@@ -57,9 +57,14 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
                         float *const *master, void *stream);
 fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
                               void *const *full_out, void *stream);
+// acc: NULL, or R fp32 gradient accumulators added to grad (rank by rank)
+// before the fold.
 fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
                             float *const *m, float *const *v, void *const *param_shard_out,
-                            float *const *grad_shard_out, const AdamScalars &c, void *stream);
+                            float *const *grad_shard_out, const AdamScalars &c, void *stream,
+                            const float *const *acc = nullptr);
+fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const void *const *grad,
+                              int first, void *stream);
 fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, void *const *out,
                               fsdp_dtype out_dtype, void *stream);
 fsdp_status launch_rs_adamw_gather(const fsdp_layout_t *A, const void *const *grad,

@@ -42,6 +42,7 @@ constexpr int kPackCtasPerSm = 8;
 // all-reduce (bf16 grads -> fp32 outputs): 1/SM 1.826, 2/SM 1.744, 3/SM
 // 1.941, 4/SM 1.904, 8/SM 1.976 ms.
 constexpr int kAllReduceCtasPerSm = 2;
+constexpr int kAccumulateCtasPerSm = 3;
 
 struct PackParams {
     const float *full;
@@ -64,6 +65,7 @@ struct GatherParams {
 
 struct RsParams {
     const void *grad[kMaxR];
+    const float *acc[kMaxR];  // gradient accumulators (NULL unless accumulating)
     float *master[kMaxR];
     float *m[kMaxR];
     float *v[kMaxR];
@@ -261,14 +263,25 @@ __device__ __forceinline__ float load_grad(const void *g, int64_t j)
 
 // Scalar path: rank-ordered fp32 fold of element j, averaged, then AdamW.
 // PP is any parameter block with grad, master, m, v, pshard, gshard, c.
-template <bool kGradBf16, bool kParamBf16, class PP>
+// Rank q's gradient at unit index j; with accumulators, the accumulated
+// earlier micro-batches plus this one (one fp32 add).
+template <bool kGradBf16, bool kAccum, class PP>
+__device__ __forceinline__ float rank_grad(const PP &p, int q, int64_t j)
+{
+    float g = load_grad<kGradBf16>(p.grad[q], j);
+    if (kAccum)
+        g = __fadd_rn(__ldcs(p.acc[q] + j), g);
+    return g;
+}
+
+template <bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_scalar(const PP &p, int R, const Tile &T, int64_t e)
 {
     const int r = T.rank;
     const int64_t j = T.fbase + e;
-    float acc = load_grad<kGradBf16>(p.grad[0], j);
+    float acc = rank_grad<kGradBf16, kAccum>(p, 0, j);
     for (int q = 1; q < R; q++)
-        acc = __fadd_rn(acc, load_grad<kGradBf16>(p.grad[q], j));
+        acc = __fadd_rn(acc, rank_grad<kGradBf16, kAccum>(p, q, j));
     const float g = __fmul_rn(acc, p.c.inv_R);
     const int64_t s = T.sbase + e;
     AdamOut o = adamw_elem(p.c, g, p.master[r][s], p.m[r][s], p.v[r][s]);
@@ -350,8 +363,28 @@ __device__ __forceinline__ void fold8(const PP &p, int R, int64_t j, float acc[8
     }
 }
 
+// The fold when rank q's gradient is accumulator q plus this micro-batch's
+// g_q: a = acc_q[j+k] + g_q[j+k], then the same left fold over ranks.
+template <int RC, bool kGradBf16, class PP>
+__device__ __forceinline__ void fold8_accum(const PP &p, int R, int64_t j, float out[8])
+{
+    const int n = RC > 0 ? RC : R;
+#pragma unroll 2
+    for (int q = 0; q < n; q++) {
+        float g[8];
+        load_grad8<kGradBf16>(p.grad[q], j, g);
+        const float4 a0 = ld_f4(p.acc[q] + j), a1 = ld_f4(p.acc[q] + j + 4);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const float x = __fadd_rn(a[k], g[k]);
+            out[k] = q == 0 ? x : __fadd_rn(out[k], x);
+        }
+    }
+}
+
 // One reduce-scatter + AdamW tile.
-template <int RC, bool kGradBf16, bool kParamBf16, class PP>
+template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
 {
     const int r = T.rank;
@@ -360,14 +393,14 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
         for (int k = 0; k < kElemsPerThread; k++) {
             int64_t e = threadIdx.x + (int64_t)k * kThreads;
             if (e < T.len)
-                rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, e);
+                rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(p, R, T, e);
         }
         return;
     }
     const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
     if (e + kElemsPerThread > T.len) {
         for (int64_t q = e; q < T.len; q++)
-            rs_adamw_scalar<kGradBf16, kParamBf16>(p, R, T, q);
+            rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(p, R, T, q);
         return;
     }
     const int64_t j = T.fbase + e;
@@ -377,7 +410,10 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
     float4 w0 = ld_f4(p.master[r] + s), w1 = ld_f4(p.master[r] + s + 4);
     float4 m0 = ld_f4(p.m[r] + s), m1 = ld_f4(p.m[r] + s + 4);
     float4 v0 = ld_f4(p.v[r] + s), v1 = ld_f4(p.v[r] + s + 4);
-    fold8<RC, kGradBf16>(p, R, j, acc);
+    if (kAccum)
+        fold8_accum<RC, kGradBf16>(p, R, j, acc);
+    else
+        fold8<RC, kGradBf16>(p, R, j, acc);
     float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -409,12 +445,59 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
     }
 }
 
-template <int RC, bool kGradBf16, bool kParamBf16>
+template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum>
 __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constant__ RsParams p)
 {
     const int R = RC > 0 ? RC : p.R;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
-        rs_adamw_tile<RC, kGradBf16, kParamBf16>(p, R, locate(p.seg, p.nseg, t, false));
+        rs_adamw_tile<RC, kGradBf16, kParamBf16, kAccum>(p, R, locate(p.seg, p.nseg, t, false));
+}
+
+// ------------------------------------------------- gradient accumulation ----
+//
+// acc[q] = g[q] (first micro-batch) or acc[q] + g[q], fp32, for every rank
+// q. Tiles run over (rank, flat unit index); tile starts are multiples of
+// kTile, so only each rank's last partial vector takes the scalar path.
+
+struct AccumParams {
+    float *acc[kMaxR];
+    const void *grad[kMaxR];
+    int R;
+    int first;
+    int64_t P;
+    int64_t tiles_per_rank;
+    int64_t total_tiles;
+};
+
+template <bool kGradBf16>
+__global__ void __launch_bounds__(kThreads) accumulate_kernel(const __grid_constant__ AccumParams p)
+{
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const int q = (int)(t / p.tiles_per_rank);
+        const int64_t base = (t - (int64_t)q * p.tiles_per_rank) * kTile;
+        const int64_t len = p.P - base < kTile ? p.P - base : kTile;
+        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+        float *a = p.acc[q];
+        if (e + kElemsPerThread <= len) {
+            const int64_t j = base + e;
+            float g[8];
+            load_grad8<kGradBf16>(p.grad[q], j, g);
+            if (!p.first) {
+                const float4 a0 = ld_f4(a + j), a1 = ld_f4(a + j + 4);
+                const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    g[k] = __fadd_rn(x[k], g[k]);
+            }
+            st_f4(a + j, make_float4(g[0], g[1], g[2], g[3]));
+            st_f4(a + j + 4, make_float4(g[4], g[5], g[6], g[7]));
+        } else {
+            for (int64_t j = base + e; j < base + len; j++) {
+                const float g = load_grad<kGradBf16>(p.grad[q], j);
+                a[j] = p.first ? g : __fadd_rn(a[j], g);
+            }
+        }
+    }
 }
 
 // --------------------------------------------------------- all-reduce ----
@@ -626,20 +709,35 @@ fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
     return FSDP_OK;
 }
 
-template <bool kGradBf16, bool kParamBf16>
+template <bool kGradBf16, bool kParamBf16, bool kAccum>
 static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
 {
+    const char *w = "rs_adamw";
     switch (R) {
-    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
-    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
-    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
-    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16>, p, s, "rs_adamw", kRsCtasPerSm);
+    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
+    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
+    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
+    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
     }
+}
+
+template <bool kAccum>
+static fsdp_status rs_dispatch_dtypes(int dev, const fsdp_layout_t *L, RsParams &p, cudaStream_t s)
+{
+    const bool gb = L->grad_dtype == FSDP_BF16, pb = L->param_dtype == FSDP_BF16;
+    if (gb && pb)
+        return rs_dispatch<true, true, kAccum>(dev, L->R, p, s);
+    if (gb)
+        return rs_dispatch<true, false, kAccum>(dev, L->R, p, s);
+    if (pb)
+        return rs_dispatch<false, true, kAccum>(dev, L->R, p, s);
+    return rs_dispatch<false, false, kAccum>(dev, L->R, p, s);
 }
 
 fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
                             float *const *m, float *const *v, void *const *param_shard_out,
-                            float *const *grad_shard_out, const AdamScalars &c, void *stream)
+                            float *const *grad_shard_out, const AdamScalars &c, void *stream,
+                            const float *const *acc)
 {
     int dev;
     fsdp_status st = select_device(master[0], &dev);
@@ -651,6 +749,7 @@ fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, flo
     p.c = c;
     for (int r = 0; r < L->R; r++) {
         p.grad[r] = grad[r];
+        p.acc[r] = acc ? acc[r] : nullptr;
         p.master[r] = master[r];
         p.m[r] = m[r];
         p.v[r] = v[r];
@@ -658,21 +757,37 @@ fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, flo
         p.gshard[r] = grad_shard_out ? grad_shard_out[r] : nullptr;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    const bool gb = L->grad_dtype == FSDP_BF16, pb = L->param_dtype == FSDP_BF16;
     for (const LaunchPlan &plan : L->valid_plans) {
         fill_segs(p, plan);
-        if (gb && pb)
-            st = rs_dispatch<true, true>(dev, L->R, p, s);
-        else if (gb)
-            st = rs_dispatch<true, false>(dev, L->R, p, s);
-        else if (pb)
-            st = rs_dispatch<false, true>(dev, L->R, p, s);
-        else
-            st = rs_dispatch<false, false>(dev, L->R, p, s);
+        st = acc ? rs_dispatch_dtypes<true>(dev, L, p, s) : rs_dispatch_dtypes<false>(dev, L, p, s);
         if (st != FSDP_OK)
             return st;
     }
     return FSDP_OK;
+}
+
+fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const void *const *grad,
+                              int first, void *stream)
+{
+    int dev;
+    fsdp_status st = select_device(acc[0], &dev);
+    if (st != FSDP_OK)
+        return st;
+    AccumParams p;
+    memset(&p, 0, sizeof p);
+    p.R = L->R;
+    p.first = first ? 1 : 0;
+    p.P = L->P;
+    p.tiles_per_rank = (L->P + kTile - 1) / kTile;
+    p.total_tiles = p.tiles_per_rank * L->R;
+    for (int r = 0; r < L->R; r++) {
+        p.acc[r] = acc[r];
+        p.grad[r] = grad[r];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L->grad_dtype == FSDP_BF16)
+        return run(dev, accumulate_kernel<true>, p, s, "accumulate", kAccumulateCtasPerSm);
+    return run(dev, accumulate_kernel<false>, p, s, "accumulate", kAccumulateCtasPerSm);
 }
 
 }  // namespace fsdp

@@ -100,3 +100,21 @@ class ShardedUnit:
         """DDP's all-reduce of the R full gradients into R full outputs
         (fp32 or bf16), for comparison with the sharded path."""
         capi.fsdp_all_reduce(self.layout, grads, out, _DT[out_dtype][0], stream)
+
+    # -- gradient accumulation over micro-batches ---------------------------
+    def alloc_accumulators(self):
+        """R fp32 full-unit gradient accumulators."""
+        return [torch.empty(self.P, dtype=torch.float32, device=self.device)
+                for _ in range(self.R)]
+
+    def accumulate_grad(self, grads, acc, first: bool, stream=None) -> None:
+        """acc = grads (first micro-batch) or acc + grads, per rank, in fp32."""
+        capi.fsdp_accumulate_grad(self.layout, acc, grads, first, stream)
+
+    def reduce_scatter_adamw_accum(self, acc, grads, hp: capi.AdamWHP, grad_shard_out=None,
+                                   step: int | None = None, stream=None) -> None:
+        """The optimizer step on acc + grads (the last micro-batch fused in)."""
+        self.step = self.step + 1 if step is None else int(step)
+        capi.fsdp_reduce_scatter_adamw_accum(self.layout, acc, grads, self.master, self.m,
+                                             self.v, self.param_shard, grad_shard_out, hp,
+                                             self.step, stream)

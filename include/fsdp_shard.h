@@ -191,6 +191,33 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
 fsdp_status fsdp_all_reduce(const fsdp_layout_t *layout, const void *const *grad_full,
                             void *const *out, fsdp_dtype out_dtype, void *stream);
 
+/* Gradient accumulation over micro-batches ("FSDP2 的参数全聚合、梯度归约分片
+ * 与显存峰值", §08: every micro-batch runs forward and backward, the update
+ * happens once per K micro-batches). For every rank q and unit element j:
+ *   first != 0:  acc_full[q][j] = g_q[j]                 (exact widening)
+ *   first == 0:  acc_full[q][j] = acc_full[q][j] + g_q[j]   (one fp32 add)
+ * acc_full[q]: rank q's P fp32 accumulators (read and written); grad_full[q]:
+ * P elements of the layout's grad_dtype. The accumulated gradient is the
+ * plain sum over micro-batches; scale the loss for any 1/K normalisation.
+ * Errors: FSDP_EINVAL, FSDP_EALIGN. */
+fsdp_status fsdp_accumulate_grad(const fsdp_layout_t *layout, float *const *acc_full,
+                                 const void *const *grad_full, int first, void *stream);
+
+/* The last micro-batch fused into the optimizer step: exactly
+ * fsdp_reduce_scatter_adamw, except that rank q's gradient is
+ * acc_full[q][j] + grad_full[q][j] (one fp32 add per rank, then the same
+ * rank-ordered fold). Bit-identical to fsdp_accumulate_grad of the last
+ * micro-batch followed by fsdp_reduce_scatter_adamw on the accumulators, and
+ * saves one write and one read of the accumulators. acc_full is read only.
+ * Errors as fsdp_reduce_scatter_adamw. */
+fsdp_status fsdp_reduce_scatter_adamw_accum(const fsdp_layout_t *layout,
+                                            const float *const *acc_full,
+                                            const void *const *grad_full, float *const *master,
+                                            float *const *m, float *const *v,
+                                            void *const *param_shard_out,
+                                            float *const *grad_shard_out, const fsdp_adamw_hp *hp,
+                                            int64_t step, void *stream);
+
 /* Message for the last non-OK status returned on the calling thread. */
 const char *fsdp_last_error(void);
 

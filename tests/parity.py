@@ -211,3 +211,60 @@ def run_overlap_case(case_rs: UnitCase, case_ag: UnitCase, seed_shift: int = 500
         if bf_a:
             assert_bf16_close(host(Ua.param_shard[r]), want_p16[r], f"overlapped bf16[{r}]")
     torch.cuda.synchronize()
+
+
+def run_accumulation_case(case: UnitCase, K: int):
+    """K micro-batches: accumulate K-1 on the GPU, fuse the last into the
+    reduce-scatter + AdamW; compare with the oracle accumulating all K and
+    reduce-scattering the accumulators. Also checks that the unfused GPU path
+    (accumulate all K, reduce-scatter fp32 accumulators) gives the same bits."""
+    w, _ = host_inputs(case)
+    micro = [host_inputs(UnitCase(**{**case.__dict__, "seed": case.seed + 17 * k}))[1]
+             for k in range(K)]
+    omode = oracle.FLAT if case.mode == "flat" else oracle.PER_PARAM
+    O = oracle.layout(omode, case.R, case.shapes)
+    U = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype)
+    bf16 = case.param_dtype == "bf16"
+    U.shard_from_full(to_dev(w))
+    masters, _ = oracle.pack(O, w, with_bf16=bf16)
+    acc = U.alloc_accumulators()
+    o_acc = [np.zeros(U.P, np.float32) for _ in range(case.R)]
+    for k in range(K - 1):
+        U.accumulate_grad([to_dev(g) for g in micro[k]], acc, first=(k == 0))
+        oracle.accumulate(o_acc, micro[k], first=(k == 0))
+    for r in range(case.R):
+        if K > 1:
+            assert_bits_equal(host(acc[r]), o_acc[r], f"accumulator[{r}]")
+    oracle.accumulate(o_acc, micro[K - 1], first=(K == 1))
+    lr, b1, b2, eps, wd = case.hp
+    gsh = [torch.zeros(U.S, dtype=torch.float32, device="cuda") for _ in range(case.R)]
+    last = [to_dev(g) for g in micro[K - 1]]
+    if K == 1:
+        for a in acc:
+            a.zero_()
+    U.reduce_scatter_adamw_accum(acc, last, AdamWHP(lr, b1, b2, eps, wd), grad_shard_out=gsh,
+                                 step=case.step)
+    m = [np.zeros(U.S, np.float32) for _ in range(case.R)]
+    v = [np.zeros(U.S, np.float32) for _ in range(case.R)]
+    want_g, want_p16 = oracle.rs_adamw(O, o_acc, masters, m, v,
+                                       oracle.AdamWHP(lr, b1, b2, eps, wd), case.step,
+                                       with_bf16=bf16)
+    for r in range(case.R):
+        assert_bits_equal(host(gsh[r]), want_g[r], f"accumulated reduce-scatter shard[{r}]")
+        assert_master_close(host(U.master[r]), masters[r], f"accumulated master[{r}]")
+        assert_moment_close(host(U.m[r]), m[r], f"accumulated m[{r}]")
+        assert_moment_close(host(U.v[r]), v[r], f"accumulated v[{r}]")
+        if bf16:
+            assert_bf16_close(host(U.param_shard[r]), want_p16[r], f"accumulated bf16[{r}]")
+    # unfused: accumulate the last micro-batch too, reduce-scatter the accumulators
+    if K > 1:
+        U.accumulate_grad(last, acc, first=False)
+        F = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, "f32")
+        F.shard_from_full(to_dev(w))
+        gsh2 = [torch.zeros(F.S, dtype=torch.float32, device="cuda") for _ in range(case.R)]
+        F.reduce_scatter_adamw(acc, AdamWHP(lr, b1, b2, eps, wd), grad_shard_out=gsh2,
+                               step=case.step)
+        for r in range(case.R):
+            assert torch.equal(gsh[r].view(torch.int32), gsh2[r].view(torch.int32))
+            assert torch.equal(U.master[r].view(torch.int32), F.master[r].view(torch.int32))
+    torch.cuda.synchronize()

@@ -256,3 +256,30 @@ def test_all_reduce_rejects_bad_arguments(lib):
     assert lib.fsdp_all_reduce(L.handle, g, _ptrs([BASE + 4 * MB, BASE + 4 * MB + (1 << 17)]),
                                capi.FSDP_F32, None) == capi.FSDP_EINVAL
     assert lib.fsdp_all_reduce(None, g, g, capi.FSDP_F32, None) == capi.FSDP_EINVAL
+
+
+def test_accumulation_rejects_bad_arguments(lib):
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(4096, 16)], capi.FSDP_BF16, capi.FSDP_BF16)
+    MB = 1 << 20
+    g = _ptrs([BASE, BASE + MB])
+    acc = _ptrs([BASE + 4 * MB, BASE + 8 * MB])
+    assert lib.fsdp_accumulate_grad(None, acc, g, 1, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_accumulate_grad(L.handle, _ptrs([BASE + 4 * MB + 8, BASE + 8 * MB]), g, 0,
+                                    None) == capi.FSDP_EALIGN
+    # an accumulator overlapping a gradient
+    assert lib.fsdp_accumulate_grad(L.handle, _ptrs([BASE + 64, BASE + 8 * MB]), g, 0,
+                                    None) == capi.FSDP_EINVAL
+    a = _rs_args()
+    # accumulators overlapping the master (an output)
+    st = lib.fsdp_reduce_scatter_adamw_accum(L.handle, a["master"], a["grad"], a["master"],
+                                             a["m"], a["v"], a["pshard"], None,
+                                             ctypes.byref(a["hp"]), 1, None)
+    assert st == capi.FSDP_EINVAL
+    st = lib.fsdp_reduce_scatter_adamw_accum(L.handle, None, a["grad"], a["master"], a["m"],
+                                             a["v"], a["pshard"], None, ctypes.byref(a["hp"]),
+                                             1, None)
+    assert st == capi.FSDP_EINVAL
+    st = lib.fsdp_reduce_scatter_adamw_accum(L.handle, acc, a["grad"], a["master"], a["m"],
+                                             a["v"], a["pshard"], None, ctypes.byref(a["hp"]),
+                                             0, None)
+    assert st == capi.FSDP_EINVAL

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from fully_sharded_state_gb300 import synth
-from parity import UnitCase, run_overlap_case, run_unit_case
+from parity import UnitCase, run_accumulation_case, run_overlap_case, run_unit_case
 
 pytestmark = pytest.mark.gpu
 
@@ -218,3 +218,19 @@ def test_all_reduce_equals_gather_of_reduce_scatter(cuda_lib, mode):
     U.all_reduce(g, out, "f32")
     for d in range(4):
         assert torch.equal(gathered[d].view(torch.int32), out[d].view(torch.int32))
+
+
+ACCUM = {
+    "block_K3": (UnitCase([(512,), (512, 512), (2048, 512)], R=4, seed=41), 3),
+    "ragged_fp32_K2": (UnitCase([(1001, 3), (7, 513), (1, 64)], R=8, param_dtype="f32",
+                                grad_dtype="f32", g_std=1.0, w_std=1.0, outlier_frac=0.01,
+                                seed=42), 2),
+    "flat_K4": (UnitCase([(1001, 3), (5, 7)], R=4, mode="flat", seed=43), 4),
+    "generic_R5_K2": (UnitCase([(513, 64), (9,)], R=5, seed=44, step=3), 2),
+    "single_micro_batch": (UnitCase([(300, 70)], R=2, seed=45), 1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ACCUM))
+def test_gradient_accumulation(cuda_lib, name):
+    run_accumulation_case(*ACCUM[name])
