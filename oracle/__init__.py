@@ -23,6 +23,7 @@ import numpy as np
 
 FLAT = 1        # FSDP1 FlatParameter
 PER_PARAM = 2   # FSDP2 per-parameter Shard(0)
+ZERO3 = 3       # ZeRO-3 inter-tensor: whole tensors on owner ranks
 F32 = 0
 BF16 = 1
 SEG_ALIGN = 8   # per-parameter shard segments are padded to a multiple of 8 elements
@@ -78,6 +79,8 @@ def _load(path: str):
     L.orc_adamw.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                             ctypes.c_void_p, ctypes.c_void_p,
                             ctypes.POINTER(ctypes.c_double), ctypes.c_int64]
+    L.orc_zero3_owners.restype = ctypes.c_int
+    L.orc_zero3_owners.argtypes = [ctypes.c_int64, ctypes.c_int64, _i64p, _i64p, _i64p]
     L.orc_owner.restype = ctypes.c_int
     L.orc_owner.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p, _i64p,
                             ctypes.c_int64, _i64p, _i64p, _i64p]
@@ -150,9 +153,12 @@ class Layout:
     full_numel: int          # P
     shard_numel: int         # per-rank shard buffer length (with padding)
     padded_numel: int        # FLAT: R * S
+    owner: np.ndarray = None  # ZERO3: owner rank of every parameter
 
     def rank_rows(self, i: int, r: int):
         """(first row, row count) of parameter i held by rank r."""
+        if self.mode == ZERO3:
+            return 0, (int(self.d0[i]) if int(self.owner[i]) == r else 0)
         start = ctypes.c_int64(0)
         cnt = lib().orc_rank_rows(int(self.d0[i]), self.R, r, ctypes.byref(start))
         return int(start.value), int(cnt)
@@ -176,8 +182,14 @@ def layout(mode: int, R: int, shapes) -> Layout:
                           _p(full_off), _p(shard_off), _p(rows), _p(out))
     if rc != 0:
         raise ValueError("oracle: bad layout arguments")
+    owner = None
+    if mode == ZERO3:
+        owner = np.zeros(max(1, n), np.int64)
+        lib().orc_zero3_owners(R, n, _p(d0 if n else _i64([0])), _p(inner if n else _i64([0])),
+                               _p(owner))
+        owner = owner[:n]
     return Layout(mode, R, [tuple(s) for s in shapes], d0, inner, full_off[:n], shard_off[:n],
-                  rows[:n], int(out[0]), int(out[1]), int(out[2]))
+                  rows[:n], int(out[0]), int(out[1]), int(out[2]), owner)
 
 
 def f32_to_bf16(x) -> np.ndarray:

@@ -87,3 +87,19 @@ def per_param_owner_ranges(shapes: list, R: int) -> list:
                 out[r].append((base + mine[0] * inner, base + (mine[-1] + 1) * inner))
         base += d0 * inner
     return out
+
+
+def zero3_parts(numels: list, R: int) -> list:
+    """ZeRO-3 inter-tensor partition ("从源码理解 FSDP", §2.1): whole tensors,
+    in order, go to the current part, which is closed once it holds at least
+    ceil(total/R) elements (the last part takes the rest). Returns the
+    list of tensor indices of every part."""
+    target = -(-sum(numels) // R)
+    parts = [[] for _ in range(R)]
+    cur, filled = 0, 0
+    for i, n in enumerate(numels):
+        parts[cur].append(i)
+        filled += n
+        if filled >= target and cur < R - 1:
+            cur, filled = cur + 1, 0
+    return parts

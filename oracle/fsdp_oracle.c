@@ -31,7 +31,10 @@
  *  - reduction: left fold over ranks 0..R-1 starting from rank 0's value,
  *    then one multiply by fl(1/R);
  *  - AdamW: decoupled weight decay first, then the moment updates and the
- *    bias-corrected step; scalars formed in double, rounded once to float.
+ *    bias-corrected step; scalars formed in double, rounded once to float;
+ *  - ZeRO-3 inter-tensor owners: tensors in unit order fill part 0 until it
+ *    holds at least ceil(P/R) elements, then part 1, and so on (the last
+ *    part takes the rest).
  */
 #include <stdint.h>
 #include <string.h>
@@ -39,6 +42,7 @@
 
 #define ORC_FLAT 1      /* FSDP1 FlatParameter */
 #define ORC_PER_PARAM 2 /* FSDP2 per-parameter Shard(0) */
+#define ORC_ZERO3 3     /* ZeRO-3 inter-tensor: whole tensors on owner ranks */
 #define ORC_F32 0
 #define ORC_BF16 1
 #define ORC_SEG_ALIGN 8
@@ -63,6 +67,43 @@ int64_t orc_rank_rows(int64_t d0, int64_t R, int64_t r, int64_t *start)
 }
 
 /* ------------------------------------------------------------------ */
+/* ZeRO-3 inter-tensor partition ([Tiny-FSDP] §2.1: each whole tensor    */
+/* is appended to parts[current_part] and recorded as that part's; §2.1  */
+/* table: balance depends on the tensor sizes). Reading for when the    */
+/* current part advances: once it holds at least ceil(P/R) elements.    */
+/* ------------------------------------------------------------------ */
+int orc_zero3_owners(int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
+                     int64_t *owner)
+{
+    int64_t total = 0;
+    for (int64_t i = 0; i < n; i++)
+        total += d0[i] * inner[i];
+    int64_t target = (total + R - 1) / R;
+    int64_t part = 0, filled = 0;
+    for (int64_t i = 0; i < n; i++) {
+        owner[i] = part;
+        filled += d0[i] * inner[i];
+        if (filled >= target && part < R - 1) {
+            part += 1;
+            filled = 0;
+        }
+    }
+    return 0;
+}
+
+/* Rows of parameter i that rank r holds: its dim-0 slice (FSDP2), or in the
+   ZeRO-3 layout every row on the owner and none elsewhere. */
+static int64_t held_rows(int mode, const int64_t *owner, const int64_t *d0, int64_t R,
+                         int64_t i, int64_t r, int64_t *start)
+{
+    if (mode == ORC_ZERO3) {
+        *start = 0;
+        return owner[i] == r ? d0[i] : 0;
+    }
+    return orc_rank_rows(d0[i], R, r, start);
+}
+
+/* ------------------------------------------------------------------ */
 /* Layout of one FSDP unit.                                           */
 /*  full_off[i]  : element offset of parameter i in the full unit      */
 /*                 (parameters concatenated row-major in unit order)  */
@@ -76,8 +117,35 @@ int64_t orc_rank_rows(int64_t d0, int64_t R, int64_t r, int64_t *start)
 int orc_layout(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *inner,
                int64_t *full_off, int64_t *shard_off, int64_t *shard_rows, int64_t *out)
 {
-    if (R < 1 || n < 0 || (mode != ORC_FLAT && mode != ORC_PER_PARAM))
+    if (R < 1 || n < 0 || (mode != ORC_FLAT && mode != ORC_PER_PARAM && mode != ORC_ZERO3))
         return -1;
+    if (mode == ORC_ZERO3) {
+        /* every tensor whole on its owner, segments padded to ORC_SEG_ALIGN;
+           every rank's buffer is as long as the longest */
+        int64_t owner[n > 0 ? n : 1], used[R];
+        for (int64_t r = 0; r < R; r++)
+            used[r] = 0;
+        for (int64_t i = 0; i < n; i++)
+            if (d0[i] < 0 || inner[i] < 0)
+                return -1;
+        orc_zero3_owners(R, n, d0, inner, owner);
+        int64_t total = 0, longest = 0;
+        for (int64_t i = 0; i < n; i++) {
+            full_off[i] = total;
+            total += d0[i] * inner[i];
+            shard_rows[i] = d0[i];
+            shard_off[i] = used[owner[i]];
+            int64_t seg = d0[i] * inner[i];
+            used[owner[i]] += (seg + ORC_SEG_ALIGN - 1) / ORC_SEG_ALIGN * ORC_SEG_ALIGN;
+        }
+        for (int64_t r = 0; r < R; r++)
+            if (used[r] > longest)
+                longest = used[r];
+        out[0] = total;
+        out[1] = longest;
+        out[2] = R * longest;
+        return 0;
+    }
     int64_t total = 0;
     int64_t seg_total = 0;
     for (int64_t i = 0; i < n; i++) {
@@ -93,7 +161,7 @@ int orc_layout(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t 
         seg_total += seg;
     }
     out[0] = total;
-    if (mode == ORC_PER_PARAM) {
+    if (mode != ORC_FLAT) {
         out[1] = seg_total;
         out[2] = R * seg_total;
     } else {
@@ -157,15 +225,18 @@ int orc_pack(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *i
     int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
     if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
         return -1;
+    int64_t owner[n > 0 ? n : 1];
+    if (mode == ORC_ZERO3)
+        orc_zero3_owners(R, n, d0, inner, owner);
     int64_t P = out[0], shard_numel = out[1];
     for (int64_t r = 0; r < R; r++) {
         float *dst = master[r];
         for (int64_t k = 0; k < shard_numel; k++)
             dst[k] = 0.0f;
-        if (mode == ORC_PER_PARAM) {
+        if (mode != ORC_FLAT) {
             for (int64_t i = 0; i < n; i++) {
                 int64_t start;
-                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                int64_t cnt = held_rows(mode, owner, d0, R, i, r, &start) * inner[i];
                 const float *src = full + full_off[i] + start * inner[i];
                 for (int64_t k = 0; k < cnt; k++)
                     dst[shard_off[i] + k] = src[k];
@@ -197,16 +268,19 @@ int orc_all_gather(int mode, int64_t R, int64_t n, const int64_t *d0, const int6
     int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
     if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
         return -1;
+    int64_t owner[n > 0 ? n : 1];
+    if (mode == ORC_ZERO3)
+        orc_zero3_owners(R, n, d0, inner, owner);
     int64_t P = out[0], S = out[1];
     for (int64_t d = 0; d < R; d++) {
         char *dst = (char *)full[d];
-        if (mode == ORC_PER_PARAM) {
+        if (mode != ORC_FLAT) {
             for (int64_t i = 0; i < n; i++) {
                 /* concatenate rank 0's rows, then rank 1's, ... */
                 int64_t pos = full_off[i];
                 for (int64_t r = 0; r < R; r++) {
                     int64_t start;
-                    int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                    int64_t cnt = held_rows(mode, owner, d0, R, i, r, &start) * inner[i];
                     if (cnt == 0)
                         continue;
                     const char *src = (const char *)shard[r] + shard_off[i] * esize;
@@ -258,16 +332,19 @@ int orc_reduce_scatter(int mode, int64_t R, int64_t n, const int64_t *d0, const 
     int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
     if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
         return -1;
+    int64_t owner[n > 0 ? n : 1];
+    if (mode == ORC_ZERO3)
+        orc_zero3_owners(R, n, d0, inner, owner);
     int64_t P = out[0], S = out[1];
     int64_t esize = grad_dtype == ORC_BF16 ? 2 : 4;
     const void *ptrs[R];
     for (int64_t r = 0; r < R; r++) {
         for (int64_t k = 0; k < S; k++)
             gshard[r][k] = 0.0f;
-        if (mode == ORC_PER_PARAM) {
+        if (mode != ORC_FLAT) {
             for (int64_t i = 0; i < n; i++) {
                 int64_t start;
-                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                int64_t cnt = held_rows(mode, owner, d0, R, i, r, &start) * inner[i];
                 int64_t j = full_off[i] + start * inner[i];
                 for (int64_t q = 0; q < R; q++)
                     ptrs[q] = (const char *)grad[q] + j * esize;
@@ -335,14 +412,17 @@ int orc_rs_adamw(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_
     int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
     if (t < 1 || orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
         return -1;
+    int64_t owner[n > 0 ? n : 1];
+    if (mode == ORC_ZERO3)
+        orc_zero3_owners(R, n, d0, inner, owner);
     if (orc_reduce_scatter(mode, R, n, d0, inner, grad_dtype, grad, gshard) != 0)
         return -1;
     int64_t P = out[0], S = out[1];
     for (int64_t r = 0; r < R; r++) {
-        if (mode == ORC_PER_PARAM) {
+        if (mode != ORC_FLAT) {
             for (int64_t i = 0; i < n; i++) {
                 int64_t start;
-                int64_t cnt = orc_rank_rows(d0[i], R, r, &start) * inner[i];
+                int64_t cnt = held_rows(mode, owner, d0, R, i, r, &start) * inner[i];
                 int64_t o = shard_off[i];
                 orc_adamw(cnt, gshard[r] + o, master[r] + o, m[r] + o, v[r] + o, hp, t);
             }
@@ -370,6 +450,9 @@ int orc_owner(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *
     int64_t full_off[n > 0 ? n : 1], shard_off[n > 0 ? n : 1], rows[n > 0 ? n : 1], out[3];
     if (orc_layout(mode, R, n, d0, inner, full_off, shard_off, rows, out) != 0)
         return -1;
+    int64_t owner[n > 0 ? n : 1];
+    if (mode == ORC_ZERO3)
+        orc_zero3_owners(R, n, d0, inner, owner);
     int64_t P = out[0], S = out[1];
     for (int64_t k = 0; k < count; k++) {
         int64_t e = j[k];
@@ -386,7 +469,7 @@ int orc_owner(int mode, int64_t R, int64_t n, const int64_t *d0, const int64_t *
         int64_t row = (e - full_off[i]) / inner[i];
         for (int64_t r = 0; r < R; r++) {
             int64_t start;
-            int64_t cnt = orc_rank_rows(d0[i], R, r, &start);
+            int64_t cnt = held_rows(mode, owner, d0, R, i, r, &start);
             if (row >= start && row < start + cnt) {
                 rank[k] = r;
                 index[k] = shard_off[i] + (e - full_off[i]) - start * inner[i];

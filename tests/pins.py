@@ -480,6 +480,62 @@ def check_accumulation_is_the_micro_batch_sum():
     assert acc[0][0] == (np.float32(1.0) + e) + e
 
 
+def check_zero3_inter_tensor_layout():
+    """ZeRO-3 inter-tensor sharding ("从源码理解 FSDP", §2.1 and its table):
+    every tensor lives whole on one owner; owners follow the brute-force
+    partition; gather(pack(W)) == W; the reduce-scatter leaves each tensor's
+    rank-averaged gradient on its owner only (== all-reduce, then the owner's
+    tensors); and on the page's own 512/8/2048 block the load is uneven,
+    while the FSDP layout gives every rank the same 786,432."""
+    rng = np.random.default_rng(37)
+    for trial in range(50):
+        shapes = _tiny_shapes(rng, max_params=6)
+        R = int(rng.integers(1, 6))
+        numels = [int(np.prod(s)) for s in shapes]
+        P = sum(numels)
+        L = oracle.layout(oracle.ZERO3, R, shapes)
+        parts = brute.zero3_parts(numels, R)
+        for r, idx in enumerate(parts):
+            for i in idx:
+                assert int(L.owner[i]) == r
+        for i in range(len(shapes)):
+            held = [L.rank_rows(i, r)[1] for r in range(R)]
+            assert sorted(held)[-1] == shapes[i][0] and sum(held) == shapes[i][0]
+        full = np.arange(1, P + 1, dtype=np.float32)
+        masters, p16 = oracle.pack(L, full, with_bf16=True)
+        for out in oracle.all_gather(L, masters):
+            assert np.array_equal(out, full)
+        base = np.cumsum([0] + numels)
+        for r in range(R):   # a rank's buffer holds exactly its tensors, padded
+            want = []
+            for i in parts[r]:
+                seg = list(range(base[i] + 1, base[i] + numels[i] + 1))
+                want += seg + [0] * (-(-numels[i] // oracle.SEG_ALIGN) * oracle.SEG_ALIGN
+                                     - numels[i])
+            want += [0] * (L.shard_numel - len(want))
+            assert masters[r].tolist() == want
+        grads = [rng.standard_normal(P).astype(np.float32) for _ in range(R)]
+        ar = oracle.all_reduce(grads, out_bf16=False)[0]
+        gsh = oracle.reduce_scatter(L, grads)
+        for r in range(R):
+            got = np.concatenate([_owned(L, r, i, gsh[r]) for i in range(len(shapes))])
+            want = np.concatenate([ar[base[i]:base[i] + numels[i]] for i in parts[r]] or
+                                  [np.zeros(0, np.float32)])
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        rank, index = oracle.owner(L, np.arange(P)) if P else (np.zeros(0), np.zeros(0))
+        for i in range(len(shapes)):
+            assert np.all(rank[base[i]:base[i + 1]] == L.owner[i])
+    g = golden("block_sharding.txt")
+    R = int(g["R"])
+    shapes = [s for _, s in _matrices_only()]
+    Z = oracle.layout(oracle.ZERO3, R, shapes)
+    F = oracle.layout(oracle.PER_PARAM, R, shapes)
+    loads = [Z.rank_numel(r) for r in range(R)]
+    assert sum(loads) == int(g["fsdp1 flat length"])
+    assert [F.rank_numel(r) for r in range(R)] == [int(g["fsdp2 total per GPU"])] * R
+    assert max(loads) > int(g["fsdp2 total per GPU"])
+
+
 def check_reduce_scatter_special_cases():
     # R = 1: the shard is the gradient itself
     g = np.array([1.5, -2.25, 3e-8, -0.0], np.float32)

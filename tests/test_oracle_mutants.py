@@ -88,6 +88,12 @@ MUTANTS = [
      "            if (0)\n                acc[q][j] = g;"),
     ("accumulation overwrites instead of adding",
      "                acc[q][j] = acc[q][j] + g;", "                acc[q][j] = g;"),
+    ("ZeRO-3 part never advances",
+     "        if (filled >= target && part < R - 1) {", "        if (0) {"),
+    ("ZeRO-3 segments not placed per owner",
+     "            shard_off[i] = used[owner[i]];", "            shard_off[i] = used[0];"),
+    ("ZeRO-3 rows held by every rank",
+     "        return owner[i] == r ? d0[i] : 0;", "        return r == 0 || owner[i] == r ? d0[i] : 0;"),
     ("bf16 widening takes the low half",
      "uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h;"),
 ]
