@@ -6,12 +6,12 @@ fused with the sharded AdamW step, over R virtual ranks held in one GPU's
 HBM. The compute path is the CUDA library ``_lib/libfsdp_shard.so``
 (C ABI in ``include/fsdp_shard.h``); ``capi`` binds it with ctypes.
 """
-from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, AdamWHP, FsdpError,
+from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, FSDP_ZERO3, AdamWHP, FsdpError,
                    LibraryNotBuilt, fsdp_accumulate_grad, fsdp_all_gather_unflatten,
                    fsdp_all_reduce, fsdp_reduce_scatter_adamw_accum, fsdp_layout, fsdp_pack_flat,
                    fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_gather, fsdp_version)
 
-__all__ = ["FSDP_BF16", "FSDP_F32", "FSDP_FLAT", "FSDP_PER_PARAM", "AdamWHP", "FsdpError",
+__all__ = ["FSDP_BF16", "FSDP_F32", "FSDP_FLAT", "FSDP_PER_PARAM", "FSDP_ZERO3", "AdamWHP", "FsdpError",
            "LibraryNotBuilt", "fsdp_accumulate_grad", "fsdp_all_gather_unflatten",
            "fsdp_all_reduce", "fsdp_reduce_scatter_adamw_accum", "fsdp_layout", "fsdp_pack_flat",
            "fsdp_reduce_scatter_adamw", "fsdp_reduce_scatter_adamw_gather", "fsdp_version",

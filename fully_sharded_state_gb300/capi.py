@@ -16,14 +16,14 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libfsdp_shard.so")
 
 FSDP_OK, FSDP_EINVAL, FSDP_EALIGN, FSDP_ERANGE, FSDP_ECUDA, FSDP_EUNSUPPORTED = 0, -1, -2, -3, -4, -5
-FSDP_FLAT, FSDP_PER_PARAM = 1, 2
+FSDP_FLAT, FSDP_PER_PARAM, FSDP_ZERO3 = 1, 2, 3
 FSDP_F32, FSDP_BF16 = 0, 1
 FSDP_MAX_RANKS = 64
 FSDP_SEG_ALIGN = 8
 
 (Q_FULL_NUMEL, Q_SHARD_NUMEL, Q_PADDED_NUMEL, Q_N_PARAMS, Q_RANKS, Q_MODE, Q_PARAM_DTYPE,
  Q_GRAD_DTYPE, Q_PARAM_FULL_OFFSET, Q_PARAM_SHARD_OFFSET, Q_PARAM_SHARD_ROWS,
- Q_PARAM_RANK_ROW_START, Q_PARAM_RANK_ROWS, Q_RANK_NUMEL) = range(14)
+ Q_PARAM_RANK_ROW_START, Q_PARAM_RANK_ROWS, Q_RANK_NUMEL, Q_PARAM_OWNER) = range(15)
 
 _STATUS_NAMES = {0: "FSDP_OK", -1: "FSDP_EINVAL", -2: "FSDP_EALIGN", -3: "FSDP_ERANGE",
                  -4: "FSDP_ECUDA", -5: "FSDP_EUNSUPPORTED"}
@@ -151,6 +151,10 @@ class Layout:
 
     def rank_numel(self, r: int) -> int:
         return self.query(Q_RANK_NUMEL, 0, r)
+
+    def param_owner(self, i: int) -> int:
+        """ZeRO-3 layouts: the rank that holds parameter i whole."""
+        return self.query(Q_PARAM_OWNER, i)
 
     def close(self):
         if self._h:

@@ -55,7 +55,11 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
     LaunchPlan cur;
     for (Seg s : segs) {
         int64_t tiles;
-        if (padded) {
+        if (s.owner >= 0) {
+            // a whole parameter on one rank: tiles over its (padded) length
+            tiles = tiles_for(padded ? s.pad_len : s.numel);
+            s.tiles_per_rank = tiles;
+        } else if (padded) {
             s.tiles_per_rank = tiles_for(s.pad_len);
             tiles = s.tiles_per_rank * R;
         } else {
@@ -81,6 +85,27 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
     return plans;
 }
 
+// ZeRO-3 owners: parameters in unit order fill rank 0 until it holds at
+// least ceil(P/R) elements, then rank 1, ...; the last rank takes the rest.
+std::vector<int64_t> zero3_owners(const std::vector<int64_t> &numel, int R)
+{
+    int64_t total = 0;
+    for (int64_t x : numel)
+        total += x;
+    const int64_t quota = ceil_div(total, R);
+    std::vector<int64_t> owner(numel.size());
+    int64_t rank = 0, held = 0;
+    for (size_t i = 0; i < numel.size(); i++) {
+        owner[i] = rank;
+        held += numel[i];
+        if (held >= quota && rank + 1 < R) {
+            ++rank;
+            held = 0;
+        }
+    }
+    return owner;
+}
+
 // Rows [start, start+count) of a dim-0 extent d0 held by rank r.
 void rank_rows(int64_t d0, int R, int r, int64_t *start, int64_t *count)
 {
@@ -92,6 +117,13 @@ void rank_rows(int64_t d0, int R, int r, int64_t *start, int64_t *count)
 
 int64_t rank_numel(const fsdp_layout_t *L, int r)
 {
+    if (L->mode == FSDP_ZERO3) {
+        int64_t tot = 0;
+        for (int i = 0; i < L->n; i++)
+            if (L->owner[i] == r)
+                tot += L->dim0[i] * L->inner[i];
+        return tot;
+    }
     if (L->mode == FSDP_FLAT)
         return std::max<int64_t>(0, std::min<int64_t>(L->shard_numel, L->P - r * L->shard_numel));
     int64_t tot = 0;
@@ -243,7 +275,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
     if (out == nullptr)
         return set_error(FSDP_EINVAL, "fsdp_layout: out is NULL");
     *out = nullptr;
-    if (mode != FSDP_FLAT && mode != FSDP_PER_PARAM)
+    if (mode != FSDP_FLAT && mode != FSDP_PER_PARAM && mode != FSDP_ZERO3)
         return set_error(FSDP_EINVAL, "fsdp_layout: unknown mode %d", (int)mode);
     if (R < 1 || R > FSDP_MAX_RANKS)
         return set_error(FSDP_EINVAL, "fsdp_layout: R = %d outside [1, %d]", R, FSDP_MAX_RANKS);
@@ -283,17 +315,34 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
         L->shard_rows.push_back(rows);
         L->shard_off.push_back(seg_total);
         if (mode == FSDP_PER_PARAM)
-            segs.push_back({P, numel, stride, seg_total, pad, 0, 0});
+            segs.push_back({P, numel, stride, seg_total, pad, 0, 0, -1});
         P += numel;
         seg_total += pad;
     }
     L->P = P;
     if (mode == FSDP_PER_PARAM) {
         L->shard_numel = seg_total;
-    } else {
+    } else if (mode == FSDP_FLAT) {
         int64_t S = ceil_div(P, R);
         L->shard_numel = S;
-        segs.push_back({0, P, S, 0, S, 0, 0});
+        segs.push_back({0, P, S, 0, S, 0, 0, -1});
+    } else {
+        std::vector<int64_t> numel(n_params);
+        for (int i = 0; i < n_params; i++)
+            numel[i] = dim0[i] * inner[i];
+        L->owner = zero3_owners(numel, R);
+        std::vector<int64_t> used(R, 0);
+        int64_t longest = 0;
+        for (int i = 0; i < n_params; i++) {
+            const int64_t o = L->owner[i];
+            const int64_t pad = ceil_div(numel[i], FSDP_SEG_ALIGN) * FSDP_SEG_ALIGN;
+            L->shard_rows[i] = dim0[i];
+            L->shard_off[i] = used[o];
+            segs.push_back({L->full_off[i], numel[i], numel[i], used[o], pad, 0, 0, o});
+            used[o] += pad;
+            longest = std::max(longest, used[o]);
+        }
+        L->shard_numel = longest;
     }
     int64_t padded;
     if (!mul_ok(L->shard_numel, R, &padded)) {
@@ -312,7 +361,8 @@ fsdp_status fsdp_layout_query(const fsdp_layout_t *L, fsdp_query what, int i, in
 {
     if (L == nullptr || out == nullptr)
         return set_error(FSDP_EINVAL, "fsdp_layout_query: NULL argument");
-    bool need_i = what >= FSDP_Q_PARAM_FULL_OFFSET && what <= FSDP_Q_PARAM_RANK_ROWS;
+    bool need_i = (what >= FSDP_Q_PARAM_FULL_OFFSET && what <= FSDP_Q_PARAM_RANK_ROWS) ||
+                  what == FSDP_Q_PARAM_OWNER;
     bool need_r = what == FSDP_Q_PARAM_RANK_ROW_START || what == FSDP_Q_PARAM_RANK_ROWS ||
                   what == FSDP_Q_RANK_NUMEL;
     if (need_i && (i < 0 || i >= L->n))
@@ -331,19 +381,30 @@ fsdp_status fsdp_layout_query(const fsdp_layout_t *L, fsdp_query what, int i, in
     case FSDP_Q_GRAD_DTYPE: *out = L->grad_dtype; break;
     case FSDP_Q_PARAM_FULL_OFFSET: *out = L->full_off[i]; break;
     case FSDP_Q_PARAM_SHARD_OFFSET:
-        if (L->mode != FSDP_PER_PARAM)
+        if (L->mode == FSDP_FLAT)
             return set_error(FSDP_EINVAL, "fsdp_layout_query: FLAT layouts have no per-parameter "
                                           "shard offset");
         *out = L->shard_off[i];
         break;
     case FSDP_Q_PARAM_SHARD_ROWS: *out = L->shard_rows[i]; break;
     case FSDP_Q_PARAM_RANK_ROW_START:
-        rank_rows(L->dim0[i], L->R, r, &a, &c);
+        if (L->mode == FSDP_ZERO3)
+            a = 0;
+        else
+            rank_rows(L->dim0[i], L->R, r, &a, &c);
         *out = a;
         break;
     case FSDP_Q_PARAM_RANK_ROWS:
-        rank_rows(L->dim0[i], L->R, r, &a, &c);
+        if (L->mode == FSDP_ZERO3)
+            c = L->owner[i] == r ? L->dim0[i] : 0;
+        else
+            rank_rows(L->dim0[i], L->R, r, &a, &c);
         *out = c;
+        break;
+    case FSDP_Q_PARAM_OWNER:
+        if (L->mode != FSDP_ZERO3)
+            return set_error(FSDP_EINVAL, "fsdp_layout_query: only ZERO3 layouts have owners");
+        *out = L->owner[i];
         break;
     case FSDP_Q_RANK_NUMEL: *out = rank_numel(L, r); break;
     default: return set_error(FSDP_EINVAL, "fsdp_layout_query: unknown query %d", (int)what);

@@ -31,6 +31,8 @@ struct Seg {
     int64_t pad_len;
     int64_t tile_begin;      // first tile of this segment within its launch
     int64_t tiles_per_rank;  // tiles of a rank that holds rank_stride (or pad_len) elements
+    int64_t owner;           // -1: dim-0 slices as above; >= 0: the whole segment
+                             // (numel elements) belongs to this rank
 };
 
 // The segments of one launch and its tile count.
@@ -82,6 +84,7 @@ struct fsdp_layout_s {
     fsdp_dtype param_dtype;
     fsdp_dtype grad_dtype;
     std::vector<int64_t> dim0, inner, full_off, shard_off, shard_rows;
+    std::vector<int64_t> owner;  // ZERO3: owner rank of each parameter
     int64_t P;            // full numel
     int64_t shard_numel;  // per-rank shard buffer numel
     std::vector<fsdp::LaunchPlan> valid_plans;   // tiles over owned elements (gather, reduce)

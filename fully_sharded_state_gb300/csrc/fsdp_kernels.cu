@@ -100,14 +100,24 @@ __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool
     }
     const Seg &s = seg[lo];
     int64_t tl = t - s.tile_begin;
-    int r = (int)(tl / s.tiles_per_rank);
-    int64_t off = (tl - (int64_t)r * s.tiles_per_rank) * kTile;
-    int64_t owned = s.numel - (int64_t)r * s.rank_stride;
-    owned = owned < 0 ? 0 : (owned > s.rank_stride ? s.rank_stride : owned);
+    int r, first_of_rank;
+    int64_t off, owned;
+    if (s.owner >= 0) {  // a whole parameter on its owner rank
+        r = (int)s.owner;
+        first_of_rank = 0;
+        off = tl * kTile;
+        owned = s.numel;
+    } else {
+        r = (int)(tl / s.tiles_per_rank);
+        first_of_rank = r;
+        off = (tl - (int64_t)r * s.tiles_per_rank) * kTile;
+        owned = s.numel - (int64_t)r * s.rank_stride;
+        owned = owned < 0 ? 0 : (owned > s.rank_stride ? s.rank_stride : owned);
+    }
     int64_t piece = padded ? s.pad_len : owned;
     Tile T;
     T.rank = r;
-    T.fbase = s.full_off + (int64_t)r * s.rank_stride + off;
+    T.fbase = s.full_off + (int64_t)first_of_rank * s.rank_stride + off;
     T.sbase = s.shard_off + off;
     T.len = piece - off < kTile ? piece - off : kTile;
     int64_t nv = owned - off;
@@ -655,6 +665,18 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
     fsdp_status st = select_device(master[0], &dev);
     if (st != FSDP_OK)
         return st;
+    if (L->mode == FSDP_ZERO3) {
+        // a rank's buffer past its own parameters is covered by no segment
+        for (int r = 0; r < L->R; r++) {
+            cudaError_t err = cudaMemsetAsync(master[r], 0, L->shard_numel * 4,
+                                              (cudaStream_t)stream);
+            if (err == cudaSuccess && param_shard)
+                err = cudaMemsetAsync(param_shard[r], 0, L->shard_numel * 2,
+                                      (cudaStream_t)stream);
+            if (err != cudaSuccess)
+                return set_error(FSDP_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(err));
+        }
+    }
     PackParams p;
     memset(&p, 0, sizeof p);
     p.full = full;

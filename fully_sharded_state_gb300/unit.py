@@ -16,7 +16,7 @@ import torch
 from . import capi
 
 _DT = {"bf16": (capi.FSDP_BF16, torch.bfloat16), "f32": (capi.FSDP_F32, torch.float32)}
-_MODE = {"flat": capi.FSDP_FLAT, "per_param": capi.FSDP_PER_PARAM}
+_MODE = {"flat": capi.FSDP_FLAT, "per_param": capi.FSDP_PER_PARAM, "zero3": capi.FSDP_ZERO3}
 
 
 class ShardedUnit:

@@ -52,6 +52,14 @@
  *        first, zero padding after.
  *      FSDP_FLAT: S = ceil(P/R); rank r holds flat elements [r*S, (r+1)*S)
  *        of the unit, the part past P being zero padding.
+ *      FSDP_ZERO3: parameters, whole and in unit order, fill rank 0 until
+ *        it holds at least ceil(P/R) elements, then rank 1, and so on, the
+ *        last rank taking the rest ("从源码理解 FSDP", §2.1: ZeRO-3 assigns
+ *        whole tensors to owner ranks; the closing rule is this library's
+ *        reading). Each rank's buffer holds its own parameters in unit
+ *        order, each segment padded to FSDP_SEG_ALIGN; every buffer is as
+ *        long as the longest. The all-gather is then the owner's broadcast
+ *        and the reduce-scatter a reduce to the owner.
  *    Padding is never part of a result: the kernels do not read it and do
  *    not write it (fsdp_pack_flat writes it as zero).
  */
@@ -75,7 +83,8 @@ typedef enum {
 
 typedef enum {
     FSDP_FLAT = 1,      /* FSDP1: one FlatParameter per unit */
-    FSDP_PER_PARAM = 2  /* FSDP2: every parameter sharded on dim 0 */
+    FSDP_PER_PARAM = 2, /* FSDP2: every parameter sharded on dim 0 */
+    FSDP_ZERO3 = 3      /* ZeRO-3 inter-tensor: every parameter whole on one owner rank */
 } fsdp_mode;
 
 typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1 } fsdp_dtype;
@@ -110,11 +119,13 @@ typedef enum {
     FSDP_Q_PARAM_DTYPE = 6,
     FSDP_Q_GRAD_DTYPE = 7,
     FSDP_Q_PARAM_FULL_OFFSET = 8,     /* (i): offset of parameter i in the full unit */
-    FSDP_Q_PARAM_SHARD_OFFSET = 9,    /* (i): PER_PARAM segment offset; FLAT: EINVAL */
-    FSDP_Q_PARAM_SHARD_ROWS = 10,     /* (i): s_i = ceil(dim0_i / R) */
+    FSDP_Q_PARAM_SHARD_OFFSET = 9,    /* (i): segment offset (ZERO3: in the owner's buffer);
+                                         FLAT: EINVAL */
+    FSDP_Q_PARAM_SHARD_ROWS = 10,     /* (i): s_i = ceil(dim0_i / R) (ZERO3: dim0_i) */
     FSDP_Q_PARAM_RANK_ROW_START = 11, /* (i, r): first dim-0 row rank r holds */
     FSDP_Q_PARAM_RANK_ROWS = 12,      /* (i, r): rows rank r holds (0 = empty) */
-    FSDP_Q_RANK_NUMEL = 13            /* (r): real (non-padding) elements rank r holds */
+    FSDP_Q_RANK_NUMEL = 13,           /* (r): real (non-padding) elements rank r holds */
+    FSDP_Q_PARAM_OWNER = 14           /* (i): ZERO3 owner rank of parameter i; else EINVAL */
 } fsdp_query;
 
 /* Read one property of the layout into *out. `i` (parameter) and `r`

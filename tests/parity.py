@@ -75,11 +75,15 @@ def assert_bf16_close(got, want, what="bf16 shard"):
     assert d.max(initial=0) <= BF16_ULP, f"{what}: max {d.max()} ulp"
 
 
+def omode(mode: str) -> int:
+    return {"flat": oracle.FLAT, "per_param": oracle.PER_PARAM, "zero3": oracle.ZERO3}[mode]
+
+
 @dataclass
 class UnitCase:
     shapes: list
     R: int
-    mode: str = "per_param"      # or "flat"
+    mode: str = "per_param"      # or "flat", "zero3"
     param_dtype: str = "bf16"
     grad_dtype: str = "bf16"
     seed: int = 0
@@ -108,8 +112,7 @@ def run_unit_case(case: UnitCase, w=None, grads=None, moments=None):
     """Pack, all-gather, reduce-scatter+AdamW, all-gather again: CUDA vs oracle."""
     if w is None:
         w, grads = host_inputs(case)
-    omode = oracle.FLAT if case.mode == "flat" else oracle.PER_PARAM
-    O = oracle.layout(omode, case.R, case.shapes)
+    O = oracle.layout(omode(case.mode), case.R, case.shapes)
     U = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype)
     assert (U.P, U.S) == (O.full_numel, O.shard_numel)
     bf16 = case.param_dtype == "bf16"
@@ -180,8 +183,7 @@ def run_overlap_case(case_rs: UnitCase, case_ag: UnitCase, seed_shift: int = 500
     w_a, grads = host_inputs(case_rs)
     case_b = UnitCase(**{**case_ag.__dict__, "seed": case_ag.seed + seed_shift})
     w_b, _ = host_inputs(case_b)
-    mk = lambda c: (oracle.layout(oracle.FLAT if c.mode == "flat" else oracle.PER_PARAM, c.R,
-                                  c.shapes),
+    mk = lambda c: (oracle.layout(omode(c.mode), c.R, c.shapes),
                     ShardedUnit(c.shapes, c.R, c.mode, c.param_dtype, c.grad_dtype))
     Oa, Ua = mk(case_rs)
     Ob, Ub = mk(case_b)
@@ -221,8 +223,7 @@ def run_accumulation_case(case: UnitCase, K: int):
     w, _ = host_inputs(case)
     micro = [host_inputs(UnitCase(**{**case.__dict__, "seed": case.seed + 17 * k}))[1]
              for k in range(K)]
-    omode = oracle.FLAT if case.mode == "flat" else oracle.PER_PARAM
-    O = oracle.layout(omode, case.R, case.shapes)
+    O = oracle.layout(omode(case.mode), case.R, case.shapes)
     U = ShardedUnit(case.shapes, case.R, case.mode, case.param_dtype, case.grad_dtype)
     bf16 = case.param_dtype == "bf16"
     U.shard_from_full(to_dev(w))

@@ -44,9 +44,13 @@ def test_library_exports_every_declared_symbol(lib):
     assert b"sm_103a" in lib.fsdp_version()
 
 
+_OMODE = {capi.FSDP_FLAT: oracle.FLAT, capi.FSDP_PER_PARAM: oracle.PER_PARAM,
+          capi.FSDP_ZERO3: oracle.ZERO3}
+
+
 def _both_layouts(mode, R, shapes, pdt=capi.FSDP_BF16, gdt=capi.FSDP_BF16):
     L = capi.fsdp_layout(mode, R, shapes, pdt, gdt)
-    O = oracle.layout(oracle.FLAT if mode == capi.FSDP_FLAT else oracle.PER_PARAM, R, shapes)
+    O = oracle.layout(_OMODE[mode], R, shapes)
     return L, O
 
 
@@ -57,8 +61,10 @@ def _compare(L, O):
     for i in range(len(O.shapes)):
         assert L.param_full_offset(i) == O.full_off[i]
         assert L.query(capi.Q_PARAM_SHARD_ROWS, i) == O.shard_rows[i]
-        if O.mode == oracle.PER_PARAM:
+        if O.mode != oracle.FLAT:
             assert L.param_shard_offset(i) == O.shard_off[i]
+        if O.mode == oracle.ZERO3:
+            assert L.param_owner(i) == O.owner[i]
         for r in range(L.R):
             s, c = O.rank_rows(i, r)
             got = L.rank_rows(i, r)
@@ -73,6 +79,7 @@ def test_layout_matches_oracle_on_workloads(lib, name):
     mode = capi.FSDP_FLAT if wl.mode == "flat" else capi.FSDP_PER_PARAM
     for u in range(len(wl.units)):
         _compare(*_both_layouts(mode, wl.R, wl.unit_shapes(u)))
+        _compare(*_both_layouts(capi.FSDP_ZERO3, wl.R, wl.unit_shapes(u)))
 
 
 def test_layout_matches_oracle_random(lib):
@@ -85,13 +92,21 @@ def test_layout_matches_oracle_random(lib):
             shapes.append(tuple([int(rng.integers(0, 300))] +
                                 [int(rng.integers(1, 70)) for _ in range(nd - 1)]))
         R = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 16, 33, 64]))
-        for mode in (capi.FSDP_PER_PARAM, capi.FSDP_FLAT):
+        for mode in (capi.FSDP_PER_PARAM, capi.FSDP_FLAT, capi.FSDP_ZERO3):
             _compare(*_both_layouts(mode, R, shapes))
 
 
 def test_layout_many_params_spans_several_launch_plans(lib):
     shapes = [(k % 7 + 1, 3) for k in range(1000)]
     _compare(*_both_layouts(capi.FSDP_PER_PARAM, 8, shapes))
+    _compare(*_both_layouts(capi.FSDP_ZERO3, 8, shapes))
+
+
+def test_owner_query_only_for_zero3(lib):
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 4, [(8, 2)], capi.FSDP_BF16, capi.FSDP_BF16)
+    out = ctypes.c_int64()
+    assert lib.fsdp_layout_query(L.handle, capi.Q_PARAM_OWNER, 0, 0, ctypes.byref(out)) == \
+        capi.FSDP_EINVAL
 
 
 # ------------------------------------------------------------------ errors --
@@ -109,7 +124,7 @@ def _raw_layout(lib, mode=capi.FSDP_PER_PARAM, R=2, dims=((4, 1),), pdt=capi.FSD
 @pytest.mark.parametrize("kw,status", [
     (dict(R=0), capi.FSDP_EINVAL),
     (dict(R=65), capi.FSDP_EINVAL),
-    (dict(mode=3), capi.FSDP_EINVAL),
+    (dict(mode=4), capi.FSDP_EINVAL),
     (dict(dims=((-1, 4),)), capi.FSDP_EINVAL),
     (dict(dims=((4, -2),)), capi.FSDP_EINVAL),
     (dict(dims=((1 << 40, 1 << 30),)), capi.FSDP_ERANGE),

@@ -234,3 +234,26 @@ ACCUM = {
 @pytest.mark.parametrize("name", sorted(ACCUM))
 def test_gradient_accumulation(cuda_lib, name):
     run_accumulation_case(*ACCUM[name])
+
+
+ZERO3 = {
+    "block_R4": UnitCase([(512,), (512, 512), (512, 512), (512, 512), (512, 512), (512,),
+                          (512, 2048), (2048, 512)], R=4, mode="zero3", seed=51),
+    "ragged_fp32_R8": UnitCase([(1001, 3), (7, 513), (1, 64), (4097, 1), (127, 513), (3, 1)], R=8,
+                               mode="zero3", param_dtype="f32", grad_dtype="f32", g_std=1.0,
+                               w_std=1.0, outlier_frac=0.01, seed=52),
+    "more_ranks_than_tensors": UnitCase([(300, 70), (9,)], R=6, mode="zero3", seed=53),
+    "R1": UnitCase([(37, 5), (8,)], R=1, mode="zero3", seed=54),
+    "many_params_step3": UnitCase([((k * 7) % 13 + 1, 8 + (k % 3)) for k in range(300)], R=8,
+                                  mode="zero3", seed=55, step=3, prior_moments=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ZERO3))
+def test_zero3_inter_tensor(cuda_lib, name):
+    run_unit_case(ZERO3[name])
+
+
+def test_zero3_prefetch_and_accumulation(cuda_lib):
+    run_overlap_case(ZERO3["block_R4"], UnitCase([(256, 40), (33, 8)], R=4, mode="zero3"))
+    run_accumulation_case(UnitCase([(513, 64), (9,), (77, 40)], R=4, mode="zero3", seed=56), 3)
