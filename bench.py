@@ -93,7 +93,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source changed since the counters were taken."""
-    path = os.path.join(HERE, "profiles", "dram_traffic__rs_adamw_all_gather.json")
+    path = os.path.join(HERE, "profiles", "dram_traffic__engine_kernels.json")
     try:
         with open(path) as f:
             d = json.load(f)

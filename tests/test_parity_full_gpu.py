@@ -106,3 +106,53 @@ def test_llama_unit_full_size_sampled(cuda_lib, u):
     U.reduce_scatter_adamw(grads, hp, grad_shard_out=gsh, step=4)
     assert_bits_equal(_at(gsh, rank, idx, dev), gs, "reduce-scatter shard at samples")
     torch.cuda.synchronize()
+
+
+def test_unit_past_two_to_the_31_elements(cuda_lib):
+    """A FlatParameter unit of 2^31 + 4,097 bf16 elements over R = 2 (about
+    47 GB on the device): element offsets and tile indices pass 2^31, so the
+    64-bit index paths run. Samples cluster around 2^31, the rank boundary
+    and the end of the unit."""
+    dev = torch.device("cuda")
+    P = (1 << 31) + 4097
+    shapes = [(P,)]
+    U = ShardedUnit(shapes, 2, "flat", "bf16", "bf16")
+    O = oracle.layout(oracle.FLAT, 2, shapes)
+    assert (U.P, U.S) == (O.full_numel, O.shard_numel)
+    for r in range(2):
+        U.param_shard[r].copy_(synth.device_normal(900 + r, U.S, 0.02, dev, torch.bfloat16))
+        U.master[r].copy_(synth.device_normal(910 + r, U.S, 0.02, dev))
+        U.m[r].copy_(synth.device_normal(920 + r, U.S, 1e-4, dev))
+        z = synth.device_normal(930 + r, U.S, 1e-3, dev)
+        U.v[r].copy_(z.mul_(z).mul_(1e-3))
+        del z
+    rng = np.random.default_rng(7)
+    js = set()
+    for c in (0, U.S - 1, U.S, 1 << 31, P - 1):
+        js.update(range(max(0, c - 40), min(P, c + 40)))
+    js.update(rng.integers(0, P, 20000).tolist())
+    js = np.array(sorted(js), np.int64)
+    rank, idx = oracle.owner(O, js)
+    jt = torch.from_numpy(js).to(dev)
+
+    full = U.alloc_full()
+    U.all_gather(full)
+    want = _at(U.param_shard, rank, idx, dev)
+    for d in range(2):
+        assert_bits_equal(host(full[d][jt]), want, f"full[{d}] past 2^31")
+    del full
+    grads = [synth.device_normal(940 + q, P, 1e-3, dev, torch.bfloat16) for q in range(2)]
+    hp = AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    ohp = oracle.AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    g_s = [host(grads[q][jt]) for q in range(2)]
+    w_s, m_s, v_s = (_at(b, rank, idx, dev) for b in (U.master, U.m, U.v))
+    U.reduce_scatter_adamw(grads, hp, step=2)
+    torch.cuda.synchronize()
+    gs = oracle.sum_ranks(g_s)
+    w_o, m_o, v_o = w_s.copy(), m_s.copy(), v_s.copy()
+    oracle.adamw(gs, w_o, m_o, v_o, ohp, 2)
+    assert_master_close(_at(U.master, rank, idx, dev), w_o)
+    assert_moment_close(_at(U.m, rank, idx, dev), m_o, "m")
+    assert_moment_close(_at(U.v, rank, idx, dev), v_o, "v")
+    assert_bf16_close(_at(U.param_shard, rank, idx, dev), oracle.f32_to_bf16(w_o))
+    torch.cuda.synchronize()
