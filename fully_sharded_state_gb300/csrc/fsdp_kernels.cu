@@ -1,15 +1,18 @@
 // fsdp_kernels.cu -- the shard engine's kernels for sm_103a (GB300).
 //
-// All three kernels stream HBM: nothing here is a dense contraction, so there
-// is no tensor-core work. They share one work decomposition: a launch covers
-// up to kMaxSegsPerLaunch segments (parameters, or one FlatParameter); each
-// segment's rank pieces are cut into tiles of kTile elements; a persistent
-// grid (a few CTAs per SM) walks the tiles in order, so at any moment the
-// grid touches one contiguous window of every buffer. Each thread owns 8
-// consecutive elements of a tile: one 16-byte vector per bf16 stream, two
-// per fp32 stream. Tiles whose start is not 8-element aligned in both the
-// full and the shard buffer (ragged FSDP1 boundaries, odd row widths) take a
-// scalar path with the same per-element arithmetic.
+// Every kernel here streams HBM: nothing is a dense contraction, so there is
+// no tensor-core work. The layout-driven kernels (pack, all-gather, fused
+// reduce-scatter + AdamW) share one work decomposition: a launch covers up to
+// kMaxSegsPerLaunch segments (parameters, one FlatParameter, or ZeRO-3 tensors
+// with their owner ranks); each segment's rank pieces are cut into tiles of
+// kTile elements; a persistent grid (a few CTAs per SM) walks the tiles in
+// order, so at any moment the grid touches one contiguous window of every
+// buffer. Each thread owns 8 consecutive elements of a tile: one 16-byte
+// vector per bf16 stream, two per fp32 stream. Tiles whose start is not
+// 8-element aligned in both the full and the shard buffer (ragged FSDP1
+// boundaries, odd row widths) take a scalar path with the same per-element
+// arithmetic. The all-reduce and gradient-accumulation kernels tile the flat
+// unit index the same way.
 //
 // Segment descriptors and the R per-rank pointers travel in the kernel
 // parameter block (__grid_constant__), so the kernels need no device memory

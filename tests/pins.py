@@ -646,4 +646,21 @@ def check_bf16_round_to_nearest_even():
     assert np.array_equal(oracle.f32_to_bf16(wide)[ok], every[ok])
 
 
+def exhaustive_bf16_rounding():
+    """fp32 -> bf16 narrowing against torch's conversion on all 2^32 bit
+    patterns (NaNs: both NaN). Kept out of ALL_CHECKS, which the mutation
+    test runs once per planted mistake; check_bf16_round_to_nearest_even
+    covers the rounding-critical patterns there."""
+    import torch
+    chunk = 1 << 26
+    for c in range((1 << 32) // chunk):
+        bits = np.arange(c * chunk, (c + 1) * chunk, dtype=np.uint64).astype(np.uint32)
+        x = bits.view(np.float32)
+        ours = oracle.f32_to_bf16(x)
+        ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        nan = np.isnan(x)
+        assert np.array_equal(ours[~nan], ref[~nan]), c
+        assert np.all(np.isnan(oracle.bf16_to_f32(ours[nan]))), c
+
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]
