@@ -10,7 +10,6 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libfsdp_shard.so")

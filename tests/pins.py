@@ -9,7 +9,6 @@ planted mistake and requires that some check fails for each.
 """
 from __future__ import annotations
 
-import itertools
 from fractions import Fraction
 from pathlib import Path
 

@@ -4,7 +4,6 @@ import json
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 import bench

@@ -10,7 +10,6 @@ import tempfile
 from concurrent.futures import ThreadPoolExecutor
 from pathlib import Path
 
-import pytest
 
 REPO = Path(__file__).resolve().parent.parent
 SRC = (REPO / "oracle" / "fsdp_oracle.c").read_text()

@@ -5,7 +5,6 @@ toy, the 512/8/2048 block (FSDP2), twelve blocks as FSDP1 FlatParameters and
 the ragged stress unit; then edge cases: R = 1, odd R, the generic-R kernels,
 empty parameters and ranks, misaligned rank boundaries, more parameters than
 one launch takes, mixed dtypes, P = 0."""
-import numpy as np
 import pytest
 import torch
 
