@@ -282,11 +282,18 @@ def run_ours(args):
     R = wl.R
     hp = AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
 
-    units, grads = [], []
+    units, grads, pack_ms = [], [], []
     for u, spec in enumerate(units_spec):
         U = ShardedUnit([s for _, s in spec], R, "per_param", "bf16", "bf16", device=dev,
                         names=[n for n, _ in spec])
-        U.shard_from_full(synth.device_normal(synth.seed("w", wl, u), U.P, wl.w_std, dev))
+        w_full = synth.device_normal(synth.seed("w", wl, u), U.P, wl.w_std, dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        U.shard_from_full(w_full)
+        b.record()
+        b.synchronize()
+        pack_ms.append(a.elapsed_time(b))
+        del w_full
         units.append(U)
         grads.append([synth.device_normal(synth.seed("g", wl, u, r), U.P, wl.g_std, dev,
                                           torch.bfloat16) for r in range(R)])
@@ -424,6 +431,13 @@ def run_ours(args):
                            "avg_launch_ms": round(rsacc_ms, 4),
                            "traffic": profiled_traffic("rs_adamw_accum", args.workload)}}
 
+    pack_bytes = U0.P * 4 + R * U0.S * (4 + 2)
+    pack = {"kernel": "pack_kernel (shard from full: fp32 master + bf16 shard; set-up, "
+                      "untimed step)", "unit": "GB/s",
+            "achieved": gbs(pack_bytes, statistics.mean(pack_ms[1:] or pack_ms)),
+            "algorithmic_bytes_per_launch": pack_bytes,
+            "avg_launch_ms": round(statistics.mean(pack_ms[1:] or pack_ms), 4)}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes)
@@ -445,7 +459,7 @@ def run_ours(args):
                            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 "pct_of_hbm_peak": round(value / world / peak, 4),
                 "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
-                "grad_accumulation": accumulation,
+                "grad_accumulation": accumulation, "pack": pack,
                 "clocks": clocks.summary(), "gpu_launches": launches,
                 "cpu_baseline": cpu, "e2e": e2e}
         print(json.dumps(line), flush=True)

@@ -166,15 +166,53 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         Tile T = locate(p.seg, p.nseg, t, true);
         float *dst = p.master[T.rank] + T.sbase;
+        uint16_t *dst16 = kBf16 ? p.pshard[T.rank] + T.sbase : nullptr;
         const float *src = p.full + T.fbase;
+        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+        const bool aligned = ((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0;
+        if (aligned && e + kElemsPerThread > T.len) {
+            // the tile's last, partial group of this thread's 8 elements
+            for (int64_t q = e; q < T.len; q++) {
+                float x = q < T.nvalid ? src[q] : 0.0f;
+                dst[q] = x;
+                if (kBf16)
+                    dst16[q] = f32_to_bf16_bits(x);
+            }
+            continue;
+        }
+        if (aligned) {
+            // 8 elements: owned ones from the full unit, the rest zero padding
+            float x[8];
+            if (e + kElemsPerThread <= T.nvalid) {
+                const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + e));
+                const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + e + 4));
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    x[k] = e + k < T.nvalid ? src[e + k] : 0.0f;
+            }
+            st_f4(dst + e, make_float4(x[0], x[1], x[2], x[3]));
+            st_f4(dst + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+            if (kBf16) {
+                uint4 v;
+                v.x = (uint32_t)f32_to_bf16_bits(x[0]) | ((uint32_t)f32_to_bf16_bits(x[1]) << 16);
+                v.y = (uint32_t)f32_to_bf16_bits(x[2]) | ((uint32_t)f32_to_bf16_bits(x[3]) << 16);
+                v.z = (uint32_t)f32_to_bf16_bits(x[4]) | ((uint32_t)f32_to_bf16_bits(x[5]) << 16);
+                v.w = (uint32_t)f32_to_bf16_bits(x[6]) | ((uint32_t)f32_to_bf16_bits(x[7]) << 16);
+                st_stream(dst16 + e, v);
+            }
+            continue;
+        }
 #pragma unroll
         for (int k = 0; k < kElemsPerThread; k++) {
-            int64_t e = threadIdx.x + (int64_t)k * kThreads;
-            if (e < T.len) {
-                float x = e < T.nvalid ? src[e] : 0.0f;
-                dst[e] = x;
+            int64_t q = threadIdx.x + (int64_t)k * kThreads;
+            if (q < T.len) {
+                float x = q < T.nvalid ? src[q] : 0.0f;
+                dst[q] = x;
                 if (kBf16)
-                    p.pshard[T.rank][T.sbase + e] = f32_to_bf16_bits(x);
+                    dst16[q] = f32_to_bf16_bits(x);
             }
         }
     }
