@@ -234,6 +234,20 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+def host_cpu() -> str:
+    """The host CPU's model as /proc/cpuinfo names it (Arm parts report an
+    implementer/part pair instead of a model name)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name", "CPU part"):
+        for line in info:
+            if line.startswith(key):
+                return f"{key}: {line.split(':', 1)[1].strip()}"
+    return "unknown"
+
+
 def cpu_baseline(wl, target_s: float = 10.0):
     smp = OracleSample(wl)
     dt = smp.run()
@@ -241,7 +255,8 @@ def cpu_baseline(wl, target_s: float = 10.0):
     total_t = dt + sum(smp.run() for _ in range(reps - 1))
     return {"value": round(reps * smp.nbytes / total_t / 1e9, 4), "unit": UNIT, "cores": 1,
             "kind": "oracle", "sample": f"{reps} runs of {smp.desc}",
-            "seconds": round(total_t, 2)}
+            "seconds": round(total_t, 2), "host_cores_available": os.cpu_count(),
+            "host_cpu": host_cpu()}
 
 
 def run_reference(args):
@@ -438,6 +453,8 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": pack_bytes,
             "avg_launch_ms": round(statistics.mean(pack_ms[1:] or pack_ms), 4)}
 
+    small = None if args.no_small else small_configs(dev, hp)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes)
@@ -460,12 +477,56 @@ def run_ours(args):
                 "pct_of_hbm_peak": round(value / world / peak, 4),
                 "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
                 "grad_accumulation": accumulation, "pack": pack,
+                "l2_resident_configs": small,
                 "clocks": clocks.summary(), "gpu_launches": launches,
                 "cpu_baseline": cpu, "e2e": e2e}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def small_configs(dev, hp):
+    """The smaller workloads, whose units fit in the 129 MB L2: one 512/8/2048
+    TransformerBlock (FSDP2, R=4) and twelve of them as FSDP1 FlatParameters
+    (R=4). Flagged as L2-resident; they are parity workloads, reported for
+    context, not the headline."""
+    import torch
+    from fully_sharded_state_gb300 import ShardedUnit, synth
+    out = {}
+    for name in ("block", "block12_flat"):
+        wl = synth.WORKLOADS[name]
+        units = [ShardedUnit(wl.unit_shapes(u), wl.R, wl.mode, "bf16", "bf16", device=dev)
+                 for u in range(len(wl.units))]
+        grads = []
+        for u, U in enumerate(units):
+            U.shard_from_full(synth.device_normal(synth.seed("w", wl, u), U.P, wl.w_std, dev))
+            grads.append([synth.device_normal(synth.seed("g", wl, u, r), U.P, wl.g_std, dev,
+                                              torch.bfloat16) for r in range(wl.R)])
+        full = [torch.empty(units[0].P, dtype=torch.bfloat16, device=dev) for _ in range(wl.R)]
+
+        def step():
+            for k, U in enumerate(units):
+                U.all_gather(full)
+                U.reduce_scatter_adamw(grads[k], hp)
+
+        for _ in range(5):
+            step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record()
+        for _ in range(50):
+            step()
+        b.record()
+        b.synchronize()
+        ms = a.elapsed_time(b) / 50
+        nbytes = sum(all_gather_bytes(U.P, wl.R) + rs_adamw_bytes(U.P, wl.R) for U in units)
+        out[name] = {"units": len(units), "params_per_unit": units[0].P, "R": wl.R,
+                     "mode": wl.mode, "ms_per_step": round(ms, 4),
+                     "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                     "l2_resident": True, "gpu_launches_per_step": 2 * len(units)}
+        del units, grads, full
+    return out
 
 
 def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
@@ -544,6 +605,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-small", action="store_true", help="skip the L2-resident configs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
