@@ -363,53 +363,15 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     ms_step = elapsed_ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    rs_avg_ms = statistics.mean(rs_ms)
-    ag_avg_ms = statistics.mean(ag_ms)
-    rs_unit_bytes = rs_bytes / len(units)
-    ag_unit_bytes = ag_bytes / len(units)
-    rs_gbs = rs_unit_bytes / (rs_avg_ms * 1e-3) / 1e9
-    ag_gbs = ag_unit_bytes / (ag_avg_ms * 1e-3) / 1e9
-    roofline = {"kernel": "rs_adamw_kernel (fused reduce-scatter + AdamW)", "bound": "hbm",
-                "achieved": round(rs_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(rs_gbs / peak, 4), "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": int(rs_unit_bytes),
-                "avg_launch_ms": round(rs_avg_ms, 4),
-                "traffic": profiled_traffic("rs_adamw", args.workload)}
-    roofline_ag = {"kernel": "all_gather_kernel (all-gather + unflatten)", "bound": "hbm",
-                   "achieved": round(ag_gbs, 1), "peak": peak, "unit": "GB/s",
-                   "frac": round(ag_gbs / peak, 4), "peak_source": peak_src,
-                   "algorithmic_bytes_per_launch": int(ag_unit_bytes),
-                   "avg_launch_ms": round(ag_avg_ms, 4),
-                   "traffic": profiled_traffic("all_gather", args.workload)}
 
-    # DDP's collective on the same unit, for comparison: all-reduce of the R
-    # bf16 gradients into R fp32 full outputs (reduce dtype fp32)
-    U0 = units[0]
-    ar_out = [torch.empty(U0.P, dtype=torch.float32, device=dev) for _ in range(R)]
-    for _ in range(3):
-        U0.all_reduce(grads[0], ar_out, "f32", stream=stream)
-    ar_ms = []
-    for _ in range(20):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        U0.all_reduce(grads[0], ar_out, "f32", stream=stream)
-        b.record(stream)
-        b.synchronize()
-        ar_ms.append(a.elapsed_time(b))
-    del ar_out
-    ar_bytes = R * U0.P * (2 + 4)
-    ar_avg = statistics.mean(ar_ms)
-    peak, peak_src = measured_peak()
-    ddp = {"kernel": "all_reduce_kernel (DDP all-reduce: bf16 grads -> fp32 outputs)",
-           "bound": "hbm", "achieved": round(ar_bytes / (ar_avg * 1e-3) / 1e9, 1), "peak": peak,
-           "unit": "GB/s", "frac": round(ar_bytes / (ar_avg * 1e-3) / 1e9 / peak, 4),
-           "algorithmic_bytes_per_launch": ar_bytes, "avg_launch_ms": round(ar_avg, 4),
-           "traffic": profiled_traffic("all_reduce", args.workload)}
-
-    # gradient accumulation on the same unit: one more micro-batch added into
-    # the fp32 accumulators, and the last micro-batch fused into the step
-    acc = U0.alloc_accumulators()
-    U0.accumulate_grad(grads[0], acc, first=True, stream=stream)
+    def entry(kernel, nbytes, ms, traffic_key):
+        """Roofline record of one kernel: algorithmic bytes per launch over its
+        mean CUDA-event launch time, against the measured HBM peak."""
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": int(nbytes), "avg_launch_ms": round(ms, 4),
+                "traffic": profiled_traffic(traffic_key, args.workload) if traffic_key else None}
 
     def timed_launches(fn, n=20):
         for _ in range(3):
@@ -424,34 +386,37 @@ def run_ours(args):
             ms.append(a.elapsed_time(b))
         return statistics.mean(ms)
 
+    roofline = entry("rs_adamw_kernel (fused reduce-scatter + AdamW)", rs_bytes / len(units),
+                     statistics.mean(rs_ms), "rs_adamw")
+    roofline_ag = entry("all_gather_kernel (all-gather + unflatten)", ag_bytes / len(units),
+                        statistics.mean(ag_ms), "all_gather")
+
+    # DDP's collective on the same unit, for comparison: all-reduce of the R
+    # bf16 gradients into R fp32 full outputs (reduce dtype fp32)
+    U0 = units[0]
+    ar_out = [torch.empty(U0.P, dtype=torch.float32, device=dev) for _ in range(R)]
+    ar_ms = timed_launches(lambda: U0.all_reduce(grads[0], ar_out, "f32", stream=stream))
+    del ar_out
+    ddp = entry("all_reduce_kernel (DDP all-reduce: bf16 grads -> fp32 outputs)",
+                R * U0.P * (2 + 4), ar_ms, "all_reduce")
+
+    # gradient accumulation on the same unit: one more micro-batch added into
+    # the fp32 accumulators, and the last micro-batch fused into the step
+    acc = U0.alloc_accumulators()
+    U0.accumulate_grad(grads[0], acc, first=True, stream=stream)
     acc_ms = timed_launches(lambda: U0.accumulate_grad(grads[0], acc, first=False, stream=stream))
     rsacc_ms = timed_launches(lambda: U0.reduce_scatter_adamw_accum(acc, grads[0], hp,
                                                                      stream=stream))
     del acc
-    acc_bytes = R * U0.P * (4 + 2 + 4)
-    rsacc_bytes = U0.P * (R * (4 + 2) + 24 + 2)
-    gbs = lambda nb, ms: round(nb / (ms * 1e-3) / 1e9, 1)
     accumulation = {
-        "accumulate": {"kernel": "accumulate_kernel (acc += bf16 micro-batch grads, R ranks)",
-                       "achieved": gbs(acc_bytes, acc_ms), "frac": round(gbs(acc_bytes, acc_ms)
-                                                                         / peak, 4),
-                       "unit": "GB/s", "algorithmic_bytes_per_launch": acc_bytes,
-                       "avg_launch_ms": round(acc_ms, 4),
-                       "traffic": profiled_traffic("accumulate", args.workload)},
-        "rs_adamw_accum": {"kernel": "rs_adamw_kernel with accumulators (last micro-batch "
-                                     "fused into reduce-scatter + AdamW)",
-                           "achieved": gbs(rsacc_bytes, rsacc_ms),
-                           "frac": round(gbs(rsacc_bytes, rsacc_ms) / peak, 4), "unit": "GB/s",
-                           "algorithmic_bytes_per_launch": rsacc_bytes,
-                           "avg_launch_ms": round(rsacc_ms, 4),
-                           "traffic": profiled_traffic("rs_adamw_accum", args.workload)}}
-
-    pack_bytes = U0.P * 4 + R * U0.S * (4 + 2)
-    pack = {"kernel": "pack_kernel (shard from full: fp32 master + bf16 shard; set-up, "
-                      "untimed step)", "unit": "GB/s",
-            "achieved": gbs(pack_bytes, statistics.mean(pack_ms[1:] or pack_ms)),
-            "algorithmic_bytes_per_launch": pack_bytes,
-            "avg_launch_ms": round(statistics.mean(pack_ms[1:] or pack_ms), 4)}
+        "accumulate": entry("accumulate_kernel (acc += bf16 micro-batch grads, R ranks)",
+                            R * U0.P * (4 + 2 + 4), acc_ms, "accumulate"),
+        "rs_adamw_accum": entry("rs_adamw_kernel with accumulators (last micro-batch fused "
+                                "into reduce-scatter + AdamW)",
+                                U0.P * (R * (4 + 2) + 24 + 2), rsacc_ms, "rs_adamw_accum")}
+    pack = entry("pack_kernel (shard from full: fp32 master + bf16 shard; set-up, untimed "
+                 "step)", U0.P * 4 + R * U0.S * (4 + 2), statistics.mean(pack_ms[1:] or pack_ms),
+                 "pack")
 
     small = None if args.no_small else small_configs(dev, hp)
 
