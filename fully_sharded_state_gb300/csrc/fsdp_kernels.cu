@@ -41,7 +41,9 @@ constexpr int kMaxR = FSDP_MAX_RANKS;
 // every buffer open at once; past these points HBM does not go faster.
 constexpr int kRsCtasPerSm = 3;
 constexpr int kGatherCtasPerSm = 2;
-constexpr int kPackCtasPerSm = 8;
+// pack (set-up): 1/SM 0.810, 2/SM 0.482, 3/SM 0.404, 4/SM 0.356, 6/SM
+// 0.421, 8/SM 0.418 ms.
+constexpr int kPackCtasPerSm = 4;
 // all-reduce (bf16 grads -> fp32 outputs): 1/SM 1.826, 2/SM 1.744, 3/SM
 // 1.941, 4/SM 1.904, 8/SM 1.976 ms.
 constexpr int kAllReduceCtasPerSm = 2;
