@@ -145,9 +145,10 @@ struct Span {
 };
 
 // Checks a host array of R device pointers. Each entry must be non-NULL
-// (when bytes > 0) and 16-byte aligned.
+// (when bytes > 0) and 16-byte aligned. `first` is the array index of
+// entry 0 in error messages (multi-unit calls pass slices of longer arrays).
 fsdp_status check_ptrs(const void *const *arr, int R, int64_t bytes, bool out, const char *what,
-                       std::vector<Span> *spans)
+                       std::vector<Span> *spans, int first = 0)
 {
     if (arr == nullptr)
         return set_error(FSDP_EINVAL, "%s: pointer array is NULL", what);
@@ -156,11 +157,12 @@ fsdp_status check_ptrs(const void *const *arr, int R, int64_t bytes, bool out, c
         if (bytes == 0)
             continue;
         if (p == nullptr)
-            return set_error(FSDP_EINVAL, "%s[%d] is NULL", what, r);
+            return set_error(FSDP_EINVAL, "%s[%d] is NULL", what, first + r);
         if (reinterpret_cast<uintptr_t>(p) & 15u)
-            return set_error(FSDP_EALIGN, "%s[%d] = %p is not 16-byte aligned", what, r, p);
+            return set_error(FSDP_EALIGN, "%s[%d] = %p is not 16-byte aligned", what, first + r,
+                             p);
         uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-        spans->push_back({lo, lo + (uintptr_t)bytes, out, what, r});
+        spans->push_back({lo, lo + (uintptr_t)bytes, out, what, first + r});
     }
     return FSDP_OK;
 }
@@ -189,13 +191,14 @@ fsdp_status check_overlap(std::vector<Span> &spans)
 }
 
 fsdp_status check_gather_args(const fsdp_layout_t *L, const void *const *shard,
-                              void *const *full_out, std::vector<Span> *spans)
+                              void *const *full_out, std::vector<Span> *spans, int first = 0)
 {
     int64_t es = esize(L->param_dtype);
-    fsdp_status st = check_ptrs(shard, L->R, L->shard_numel * es, false, "shard", spans);
+    fsdp_status st = check_ptrs(shard, L->R, L->shard_numel * es, false, "shard", spans, first);
     if (st != FSDP_OK)
         return st;
-    return check_ptrs((const void *const *)full_out, L->R, L->P * es, true, "full_out", spans);
+    return check_ptrs((const void *const *)full_out, L->R, L->P * es, true, "full_out", spans,
+                      first);
 }
 
 fsdp_status check_hp(const fsdp_adamw_hp *hp, int64_t step)
@@ -214,31 +217,66 @@ fsdp_status check_hp(const fsdp_adamw_hp *hp, int64_t step)
 fsdp_status check_rs_args(const fsdp_layout_t *L, const void *const *grad_full,
                           float *const *master, float *const *m, float *const *v,
                           void *const *param_shard_out, float *const *grad_shard_out,
-                          std::vector<Span> *spans)
+                          std::vector<Span> *spans, int first = 0)
 {
     fsdp_status st;
     int64_t sb = L->shard_numel * 4;
     if ((st = check_ptrs(grad_full, L->R, L->P * esize(L->grad_dtype), false, "grad_full",
-                         spans)) != FSDP_OK)
+                         spans, first)) != FSDP_OK)
         return st;
-    if ((st = check_ptrs((const void *const *)master, L->R, sb, true, "master", spans)) != FSDP_OK)
+    if ((st = check_ptrs((const void *const *)master, L->R, sb, true, "master", spans, first)) !=
+        FSDP_OK)
         return st;
-    if ((st = check_ptrs((const void *const *)m, L->R, sb, true, "m", spans)) != FSDP_OK)
+    if ((st = check_ptrs((const void *const *)m, L->R, sb, true, "m", spans, first)) != FSDP_OK)
         return st;
-    if ((st = check_ptrs((const void *const *)v, L->R, sb, true, "v", spans)) != FSDP_OK)
+    if ((st = check_ptrs((const void *const *)v, L->R, sb, true, "v", spans, first)) != FSDP_OK)
         return st;
     if (L->param_dtype == FSDP_BF16) {
         if ((st = check_ptrs((const void *const *)param_shard_out, L->R, L->shard_numel * 2, true,
-                             "param_shard_out", spans)) != FSDP_OK)
+                             "param_shard_out", spans, first)) != FSDP_OK)
             return st;
     } else if (param_shard_out != nullptr) {
         return set_error(FSDP_EINVAL, "param_shard_out must be NULL for an F32 layout");
     }
     if (grad_shard_out != nullptr &&
         (st = check_ptrs((const void *const *)grad_shard_out, L->R, sb, true, "grad_shard_out",
-                         spans)) != FSDP_OK)
+                         spans, first)) != FSDP_OK)
         return st;
     return FSDP_OK;
+}
+
+// A multi-unit call's layouts: n >= 1, none NULL, all with the first one's
+// R and dtypes.
+fsdp_status check_units(int n, const fsdp_layout_t *const *Ls, const char *fn)
+{
+    if (n < 1 || Ls == nullptr)
+        return set_error(FSDP_EINVAL, "%s: need n_units >= 1 layouts (n_units = %d)", fn, n);
+    for (int u = 0; u < n; u++) {
+        if (Ls[u] == nullptr)
+            return set_error(FSDP_EINVAL, "%s: layouts[%d] is NULL", fn, u);
+        if (Ls[u]->R != Ls[0]->R || Ls[u]->param_dtype != Ls[0]->param_dtype ||
+            Ls[u]->grad_dtype != Ls[0]->grad_dtype)
+            return set_error(FSDP_EINVAL, "%s: layouts[%d] differs from layouts[0] in R or dtypes",
+                             fn, u);
+        if ((int64_t)n * Ls[0]->R > (int64_t)1 << 30)
+            return set_error(FSDP_ERANGE, "%s: too many units", fn);
+    }
+    return FSDP_OK;
+}
+
+// Appends entries [u*R, (u+1)*R) of a per-rank pointer array (or nothing for
+// a NULL array).
+template <typename T>
+void take(std::vector<T> &dst, T const *src, int u, int R)
+{
+    if (src)
+        dst.insert(dst.end(), src + (size_t)u * R, src + (size_t)(u + 1) * R);
+}
+
+template <typename T>
+T const *data_or_null(const std::vector<T> &v, const void *given)
+{
+    return given ? v.data() : nullptr;
 }
 
 // AdamW scalars formed in double from hp and step, rounded once to fp32.
@@ -315,7 +353,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
         L->shard_rows.push_back(rows);
         L->shard_off.push_back(seg_total);
         if (mode == FSDP_PER_PARAM)
-            segs.push_back({P, numel, stride, seg_total, pad, 0, 0, -1});
+            segs.push_back({P, numel, stride, seg_total, pad, 0, 0, -1, 0});
         P += numel;
         seg_total += pad;
     }
@@ -325,7 +363,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
     } else if (mode == FSDP_FLAT) {
         int64_t S = ceil_div(P, R);
         L->shard_numel = S;
-        segs.push_back({0, P, S, 0, S, 0, 0, -1});
+        segs.push_back({0, P, S, 0, S, 0, 0, -1, 0});
     } else {
         std::vector<int64_t> numel(n_params);
         for (int i = 0; i < n_params; i++)
@@ -338,7 +376,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
             const int64_t pad = ceil_div(numel[i], FSDP_SEG_ALIGN) * FSDP_SEG_ALIGN;
             L->shard_rows[i] = dim0[i];
             L->shard_off[i] = used[o];
-            segs.push_back({L->full_off[i], numel[i], numel[i], used[o], pad, 0, 0, o});
+            segs.push_back({L->full_off[i], numel[i], numel[i], used[o], pad, 0, 0, (int32_t)o, 0});
             used[o] += pad;
             longest = std::max(longest, used[o]);
         }
@@ -457,7 +495,7 @@ fsdp_status fsdp_all_gather_unflatten(const fsdp_layout_t *L, const void *const 
         st = check_overlap(spans);
     if (st != FSDP_OK)
         return st;
-    return launch_all_gather(L, shard, full_out, stream);
+    return launch_all_gather(1, &L, shard, full_out, stream);
 }
 
 fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *L, const void *const *grad_full,
@@ -476,8 +514,8 @@ fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *L, const void *const 
         st = check_overlap(spans);
     if (st != FSDP_OK)
         return st;
-    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
-                           adam_scalars(hp, step, L->R), stream);
+    return launch_rs_adamw(1, &L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                           adam_scalars(hp, step, L->R), stream, nullptr);
 }
 
 fsdp_status fsdp_reduce_scatter_adamw_gather(
@@ -501,10 +539,10 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
     if (st != FSDP_OK)
         return st;
     if (L->P == 0)
-        return G->P == 0 ? FSDP_OK : launch_all_gather(G, shard, full_out, stream);
+        return G->P == 0 ? FSDP_OK : launch_all_gather(1, &G, shard, full_out, stream);
     if (G->P == 0)
-        return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
-                               adam_scalars(hp, step, L->R), stream);
+        return launch_rs_adamw(1, &L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+                               adam_scalars(hp, step, L->R), stream, nullptr);
     return launch_rs_adamw_gather(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
                                   adam_scalars(hp, step, L->R), G, shard, full_out, stream);
 }
@@ -570,8 +608,94 @@ fsdp_status fsdp_reduce_scatter_adamw_accum(const fsdp_layout_t *L, const float 
         st = check_overlap(spans);
     if (st != FSDP_OK)
         return st;
-    return launch_rs_adamw(L, grad_full, master, m, v, param_shard_out, grad_shard_out,
+    return launch_rs_adamw(1, &L, grad_full, master, m, v, param_shard_out, grad_shard_out,
                            adam_scalars(hp, step, L->R), stream, acc_full);
+}
+
+
+fsdp_status fsdp_all_gather_unflatten_units(int n_units, const fsdp_layout_t *const *layouts,
+                                            const void *const *shard, void *const *full_out,
+                                            void *stream)
+{
+    const char *fn = "fsdp_all_gather_unflatten_units";
+    fsdp_status st = check_units(n_units, layouts, fn);
+    if (st != FSDP_OK)
+        return st;
+    if (shard == nullptr || full_out == nullptr)
+        return set_error(FSDP_EINVAL, "%s: pointer array is NULL", fn);
+    const int R = layouts[0]->R;
+    std::vector<Span> spans;
+    std::vector<const fsdp_layout_t *> Ls;
+    std::vector<const void *> sh;
+    std::vector<void *> fo;
+    for (int u = 0; u < n_units; u++) {
+        const fsdp_layout_t *L = layouts[u];
+        if (L->P == 0)
+            continue;  // an empty unit's pointers are not used
+        st = check_gather_args(L, shard + (size_t)u * R, full_out + (size_t)u * R, &spans, u * R);
+        if (st != FSDP_OK)
+            return st;
+        Ls.push_back(L);
+        take(sh, shard, u, R);
+        take(fo, full_out, u, R);
+    }
+    if (Ls.empty())
+        return FSDP_OK;
+    if ((st = check_overlap(spans)) != FSDP_OK)
+        return st;
+    return launch_all_gather((int)Ls.size(), Ls.data(), sh.data(), fo.data(), stream);
+}
+
+fsdp_status fsdp_reduce_scatter_adamw_units(int n_units, const fsdp_layout_t *const *layouts,
+                                            const void *const *grad_full, float *const *master,
+                                            float *const *m, float *const *v,
+                                            void *const *param_shard_out,
+                                            float *const *grad_shard_out, const fsdp_adamw_hp *hp,
+                                            int64_t step, void *stream)
+{
+    const char *fn = "fsdp_reduce_scatter_adamw_units";
+    fsdp_status st = check_units(n_units, layouts, fn);
+    if (st == FSDP_OK)
+        st = check_hp(hp, step);
+    if (st != FSDP_OK)
+        return st;
+    if (grad_full == nullptr || master == nullptr || m == nullptr || v == nullptr)
+        return set_error(FSDP_EINVAL, "%s: pointer array is NULL", fn);
+    const bool bf16 = layouts[0]->param_dtype == FSDP_BF16;
+    if (bf16 != (param_shard_out != nullptr))
+        return set_error(FSDP_EINVAL, "%s: param_shard_out must be given for BF16 layouts and "
+                                      "NULL for F32 layouts", fn);
+    const int R = layouts[0]->R;
+    std::vector<Span> spans;
+    std::vector<const fsdp_layout_t *> Ls;
+    std::vector<const void *> g;
+    std::vector<float *> ma, mm, vv, gs;
+    std::vector<void *> ps;
+    for (int u = 0; u < n_units; u++) {
+        const fsdp_layout_t *L = layouts[u];
+        if (L->P == 0)
+            continue;
+        const size_t o = (size_t)u * R;
+        st = check_rs_args(L, grad_full + o, master + o, m + o, v + o,
+                           param_shard_out ? param_shard_out + o : nullptr,
+                           grad_shard_out ? grad_shard_out + o : nullptr, &spans, u * R);
+        if (st != FSDP_OK)
+            return st;
+        Ls.push_back(L);
+        take(g, grad_full, u, R);
+        take(ma, master, u, R);
+        take(mm, m, u, R);
+        take(vv, v, u, R);
+        take(ps, param_shard_out, u, R);
+        take(gs, grad_shard_out, u, R);
+    }
+    if (Ls.empty())
+        return FSDP_OK;
+    if ((st = check_overlap(spans)) != FSDP_OK)
+        return st;
+    return launch_rs_adamw((int)Ls.size(), Ls.data(), g.data(), ma.data(), mm.data(), vv.data(),
+                           data_or_null(ps, param_shard_out), data_or_null(gs, grad_shard_out),
+                           adam_scalars(hp, step, R), stream, nullptr);
 }
 
 }  // extern "C"

@@ -31,8 +31,10 @@ struct Seg {
     int64_t pad_len;
     int64_t tile_begin;      // first tile of this segment within its launch
     int64_t tiles_per_rank;  // tiles of a rank that holds rank_stride (or pad_len) elements
-    int64_t owner;           // -1: dim-0 slices as above; >= 0: the whole segment
+    int32_t owner;           // -1: dim-0 slices as above; >= 0: the whole segment
                              // (numel elements) belongs to this rank
+    int32_t base;            // where this segment's unit starts in the launch's per-rank
+                             // pointer arrays: rank r's buffer is entry base + r
 };
 
 // The segments of one launch and its tile count.
@@ -57,14 +59,17 @@ fsdp_status set_error(fsdp_status st, const char *fmt, ...);
 // Kernel launchers (fsdp_kernels.cu). Arguments are validated by the caller.
 fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *param_shard,
                         float *const *master, void *stream);
-fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
+// The gather and the reduce-scatter take n >= 1 layouts with the same R and
+// dtypes; every per-rank pointer array then holds n*R entries, unit-major
+// (entry u*R + r is unit u's rank r).
+fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void *const *shard,
                               void *const *full_out, void *stream);
-// acc: NULL, or R fp32 gradient accumulators added to grad (rank by rank)
+// acc: NULL, or fp32 gradient accumulators added to grad (rank by rank)
 // before the fold.
-fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
-                            float *const *m, float *const *v, void *const *param_shard_out,
-                            float *const *grad_shard_out, const AdamScalars &c, void *stream,
-                            const float *const *acc = nullptr);
+fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *const *grad,
+                            float *const *master, float *const *m, float *const *v,
+                            void *const *param_shard_out, float *const *grad_shard_out,
+                            const AdamScalars &c, void *stream, const float *const *acc);
 fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const void *const *grad,
                               int first, void *stream);
 fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, void *const *out,

@@ -86,7 +86,8 @@ struct RsParams {
 // ---------------------------------------------------------------- tiles ----
 
 struct Tile {
-    int rank;
+    int rank;        // the tile's rank within its unit
+    int base;        // the unit's first entry in the per-rank pointer arrays
     int64_t fbase;   // full-buffer index of the tile's first element
     int64_t sbase;   // shard-buffer index of the tile's first element
     int64_t len;     // elements in the tile
@@ -122,6 +123,7 @@ __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool
     int64_t piece = padded ? s.pad_len : owned;
     Tile T;
     T.rank = r;
+    T.base = s.base;
     T.fbase = s.full_off + (int64_t)first_of_rank * s.rank_stride + off;
     T.sbase = s.shard_off + off;
     T.len = piece - off < kTile ? piece - off : kTile;
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
 {
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         Tile T = locate(p.seg, p.nseg, t, true);
-        float *dst = p.master[T.rank] + T.sbase;
-        uint16_t *dst16 = kBf16 ? p.pshard[T.rank] + T.sbase : nullptr;
+        float *dst = p.master[T.base + T.rank] + T.sbase;
+        uint16_t *dst16 = kBf16 ? p.pshard[T.base + T.rank] + T.sbase : nullptr;
         const float *src = p.full + T.fbase;
         const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
         const bool aligned = ((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0;
@@ -234,7 +236,8 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
 {
     using E = typename ElemOf<kEB>::T;
     constexpr int kVecs = kElemsPerThread * kEB / 16;  // 16-byte vectors per thread
-    const E *src = reinterpret_cast<const E *>(p.shard[T.rank]) + T.sbase;
+    const E *src = reinterpret_cast<const E *>(p.shard[T.base + T.rank]) + T.sbase;
+    unsigned char *const *full = p.full + T.base;
     if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0) {
         const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
         if (e + kElemsPerThread <= T.len) {
@@ -245,14 +248,14 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
             if (RC > 0) {
 #pragma unroll
                 for (int d = 0; d < (RC > 0 ? RC : 1); d++) {
-                    E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+                    E *dst = reinterpret_cast<E *>(full[d]) + T.fbase + e;
 #pragma unroll
                     for (int k = 0; k < kVecs; k++)
                         st_stream(dst + k * (16 / kEB), x[k]);
                 }
             } else {
                 for (int d = 0; d < R; d++) {
-                    E *dst = reinterpret_cast<E *>(p.full[d]) + T.fbase + e;
+                    E *dst = reinterpret_cast<E *>(full[d]) + T.fbase + e;
 #pragma unroll
                     for (int k = 0; k < kVecs; k++)
                         st_stream(dst + k * (16 / kEB), x[k]);
@@ -263,7 +266,7 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
         for (int64_t q = e; q < T.len; q++) {
             E x = src[q];
             for (int d = 0; d < R; d++)
-                reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+                reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
         }
         return;
     }
@@ -273,7 +276,7 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
         if (q < T.len) {
             E x = src[q];
             for (int d = 0; d < R; d++)
-                reinterpret_cast<E *>(p.full[d])[T.fbase + q] = x;
+                reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
         }
     }
 }
@@ -314,37 +317,53 @@ __device__ __forceinline__ float load_grad(const void *g, int64_t j)
     return __ldcs(reinterpret_cast<const float *>(g) + j);
 }
 
-// Scalar path: rank-ordered fp32 fold of element j, averaged, then AdamW.
-// PP is any parameter block with grad, master, m, v, pshard, gshard, c.
+// The R gradient (and accumulator) pointers of one unit, and the state
+// buffers of the rank that owns a tile.
+struct RankPtrs {
+    const void *const *grad;  // [R]: each rank's full local gradient
+    const float *const *acc;  // [R]: accumulators (only read when accumulating)
+    float *master, *m, *v;
+    uint16_t *pshard;
+    float *gshard;
+};
+
+template <class PP>
+__device__ __forceinline__ RankPtrs rank_ptrs(const PP &p, const Tile &T)
+{
+    const int i = T.base + T.rank;
+    return {p.grad + T.base, p.acc + T.base, p.master[i], p.m[i], p.v[i], p.pshard[i],
+            p.gshard[i]};
+}
+
 // Rank q's gradient at unit index j; with accumulators, the accumulated
 // earlier micro-batches plus this one (one fp32 add).
-template <bool kGradBf16, bool kAccum, class PP>
-__device__ __forceinline__ float rank_grad(const PP &p, int q, int64_t j)
+template <bool kGradBf16, bool kAccum>
+__device__ __forceinline__ float rank_grad(const RankPtrs &b, int q, int64_t j)
 {
-    float g = load_grad<kGradBf16>(p.grad[q], j);
+    float g = load_grad<kGradBf16>(b.grad[q], j);
     if (kAccum)
-        g = __fadd_rn(__ldcs(p.acc[q] + j), g);
+        g = __fadd_rn(__ldcs(b.acc[q] + j), g);
     return g;
 }
 
-template <bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
-__device__ __forceinline__ void rs_adamw_scalar(const PP &p, int R, const Tile &T, int64_t e)
+// Scalar path: rank-ordered fp32 fold of element j, averaged, then AdamW on
+// shard element s.
+template <bool kGradBf16, bool kParamBf16, bool kAccum>
+__device__ __forceinline__ void rs_adamw_scalar(const RankPtrs &b, const AdamScalars &c, int R,
+                                                int64_t j, int64_t s)
 {
-    const int r = T.rank;
-    const int64_t j = T.fbase + e;
-    float acc = rank_grad<kGradBf16, kAccum>(p, 0, j);
+    float acc = rank_grad<kGradBf16, kAccum>(b, 0, j);
     for (int q = 1; q < R; q++)
-        acc = __fadd_rn(acc, rank_grad<kGradBf16, kAccum>(p, q, j));
-    const float g = __fmul_rn(acc, p.c.inv_R);
-    const int64_t s = T.sbase + e;
-    AdamOut o = adamw_elem(p.c, g, p.master[r][s], p.m[r][s], p.v[r][s]);
-    p.master[r][s] = o.w;
-    p.m[r][s] = o.m;
-    p.v[r][s] = o.v;
+        acc = __fadd_rn(acc, rank_grad<kGradBf16, kAccum>(b, q, j));
+    const float g = __fmul_rn(acc, c.inv_R);
+    AdamOut o = adamw_elem(c, g, b.master[s], b.m[s], b.v[s]);
+    b.master[s] = o.w;
+    b.m[s] = o.m;
+    b.v[s] = o.v;
     if (kParamBf16)
-        p.pshard[r][s] = f32_to_bf16_bits(o.w);
-    if (p.gshard[r])
-        p.gshard[r][s] = g;
+        b.pshard[s] = f32_to_bf16_bits(o.w);
+    if (b.gshard)
+        b.gshard[s] = g;
 }
 
 __device__ __forceinline__ void unpack_bf16x8(uint4 x, float out[8])
@@ -371,16 +390,16 @@ __device__ __forceinline__ void load_grad8(const void *g, int64_t j, float out[8
 
 // Rank-ordered fp32 fold of the 8 gradient elements starting at unit index j
 // (8-aligned): acc[k] = g_0[j+k] + g_1[j+k] + ... + g_{R-1}[j+k], one rounding
-// per add. PP is any parameter block with `grad`.
-template <int RC, bool kGradBf16, class PP>
-__device__ __forceinline__ void fold8(const PP &p, int R, int64_t j, float acc[8])
+// per add. grad[q] is rank q's full gradient.
+template <int RC, bool kGradBf16>
+__device__ __forceinline__ void fold8(const void *const *grad, int R, int64_t j, float acc[8])
 {
     if (RC > 0 && kGradBf16) {
         constexpr int kR = RC > 0 ? RC : 1;
         uint4 raw[kR];  // all R loads in flight before the first add
 #pragma unroll
         for (int q = 0; q < kR; q++)
-            raw[q] = ld_stream(reinterpret_cast<const uint16_t *>(p.grad[q]) + j);
+            raw[q] = ld_stream(reinterpret_cast<const uint16_t *>(grad[q]) + j);
         unpack_bf16x8(raw[0], acc);
 #pragma unroll
         for (int q = 1; q < kR; q++) {
@@ -395,7 +414,7 @@ __device__ __forceinline__ void fold8(const PP &p, int R, int64_t j, float acc[8
         float g[kR][8];
 #pragma unroll
         for (int q = 0; q < kR; q++)
-            load_grad8<kGradBf16>(p.grad[q], j, g[q]);
+            load_grad8<kGradBf16>(grad[q], j, g[q]);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
             float a = g[0][k];
@@ -405,10 +424,10 @@ __device__ __forceinline__ void fold8(const PP &p, int R, int64_t j, float acc[8
             acc[k] = a;
         }
     } else {
-        load_grad8<kGradBf16>(p.grad[0], j, acc);
+        load_grad8<kGradBf16>(grad[0], j, acc);
         for (int q = 1; q < R; q++) {
             float g[8];
-            load_grad8<kGradBf16>(p.grad[q], j, g);
+            load_grad8<kGradBf16>(grad[q], j, g);
 #pragma unroll
             for (int k = 0; k < 8; k++)
                 acc[k] = __fadd_rn(acc[k], g[k]);
@@ -418,15 +437,15 @@ __device__ __forceinline__ void fold8(const PP &p, int R, int64_t j, float acc[8
 
 // The fold when rank q's gradient is accumulator q plus this micro-batch's
 // g_q: a = acc_q[j+k] + g_q[j+k], then the same left fold over ranks.
-template <int RC, bool kGradBf16, class PP>
-__device__ __forceinline__ void fold8_accum(const PP &p, int R, int64_t j, float out[8])
+template <int RC, bool kGradBf16>
+__device__ __forceinline__ void fold8_accum(const RankPtrs &b, int R, int64_t j, float out[8])
 {
     const int n = RC > 0 ? RC : R;
 #pragma unroll 2
     for (int q = 0; q < n; q++) {
         float g[8];
-        load_grad8<kGradBf16>(p.grad[q], j, g);
-        const float4 a0 = ld_f4(p.acc[q] + j), a1 = ld_f4(p.acc[q] + j + 4);
+        load_grad8<kGradBf16>(b.grad[q], j, g);
+        const float4 a0 = ld_f4(b.acc[q] + j), a1 = ld_f4(b.acc[q] + j + 4);
         const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
         for (int k = 0; k < 8; k++) {
@@ -440,33 +459,34 @@ __device__ __forceinline__ void fold8_accum(const PP &p, int R, int64_t j, float
 template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
 {
-    const int r = T.rank;
+    const RankPtrs b = rank_ptrs(p, T);
     if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
 #pragma unroll 1
         for (int k = 0; k < kElemsPerThread; k++) {
             int64_t e = threadIdx.x + (int64_t)k * kThreads;
             if (e < T.len)
-                rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(p, R, T, e);
+                rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(b, p.c, R, T.fbase + e,
+                                                               T.sbase + e);
         }
         return;
     }
     const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
     if (e + kElemsPerThread > T.len) {
         for (int64_t q = e; q < T.len; q++)
-            rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(p, R, T, q);
+            rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(b, p.c, R, T.fbase + q, T.sbase + q);
         return;
     }
     const int64_t j = T.fbase + e;
     const int64_t s = T.sbase + e;
     // issue every load of this thread before any arithmetic
     float acc[8];
-    float4 w0 = ld_f4(p.master[r] + s), w1 = ld_f4(p.master[r] + s + 4);
-    float4 m0 = ld_f4(p.m[r] + s), m1 = ld_f4(p.m[r] + s + 4);
-    float4 v0 = ld_f4(p.v[r] + s), v1 = ld_f4(p.v[r] + s + 4);
+    float4 w0 = ld_f4(b.master + s), w1 = ld_f4(b.master + s + 4);
+    float4 m0 = ld_f4(b.m + s), m1 = ld_f4(b.m + s + 4);
+    float4 v0 = ld_f4(b.v + s), v1 = ld_f4(b.v + s + 4);
     if (kAccum)
-        fold8_accum<RC, kGradBf16>(p, R, j, acc);
+        fold8_accum<RC, kGradBf16>(b, R, j, acc);
     else
-        fold8<RC, kGradBf16>(p, R, j, acc);
+        fold8<RC, kGradBf16>(b.grad, R, j, acc);
     float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -478,23 +498,23 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
         mv[k] = o.m;
         vv[k] = o.v;
     }
-    st_f4(p.master[r] + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
-    st_f4(p.master[r] + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
-    st_f4(p.m[r] + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
-    st_f4(p.m[r] + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
-    st_f4(p.v[r] + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
-    st_f4(p.v[r] + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    st_f4(b.master + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
+    st_f4(b.master + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
+    st_f4(b.m + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
+    st_f4(b.m + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
+    st_f4(b.v + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    st_f4(b.v + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
     if (kParamBf16) {
-        uint4 b;
-        b.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
-        b.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
-        b.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
-        b.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
-        st_stream(p.pshard[r] + s, b);
+        uint4 o;
+        o.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
+        o.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
+        o.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
+        st_stream(b.pshard + s, o);
     }
-    if (p.gshard[r]) {
-        st_f4(p.gshard[r] + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
-        st_f4(p.gshard[r] + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    if (b.gshard) {
+        st_f4(b.gshard + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_f4(b.gshard + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
     }
 }
 
@@ -580,7 +600,7 @@ __global__ void __launch_bounds__(kThreads) all_reduce_kernel(const __grid_const
         if (e + kElemsPerThread <= len) {
             const int64_t j = base + e;
             float acc[8];
-            fold8<RC, kGradBf16>(p, R, j, acc);
+            fold8<RC, kGradBf16>(p.grad, R, j, acc);
 #pragma unroll
             for (int k = 0; k < 8; k++)
                 acc[k] = __fmul_rn(acc[k], p.inv_R);
@@ -627,23 +647,43 @@ struct DeviceInfo {
 std::mutex g_dev_mu;
 std::unordered_map<int, DeviceInfo> g_dev;
 
-// Selects the device that owns `p` on this thread and returns it in *dev.
-fsdp_status select_device(const void *p, int *dev)
-{
-    cudaPointerAttributes a;
-    cudaError_t err = cudaPointerGetAttributes(&a, p);
-    if (err != cudaSuccess)
-        return set_error(FSDP_ECUDA, "cudaPointerGetAttributes: %s", cudaGetErrorString(err));
-    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
-        return set_error(FSDP_EINVAL, "output buffer %p is not device memory", p);
-    int cur = -1;
-    if ((err = cudaGetDevice(&cur)) != cudaSuccess)
-        return set_error(FSDP_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
-    if (cur != a.device && (err = cudaSetDevice(a.device)) != cudaSuccess)
-        return set_error(FSDP_ECUDA, "cudaSetDevice: %s", cudaGetErrorString(err));
-    *dev = a.device;
-    return FSDP_OK;
-}
+// Makes the device that owns a buffer current for the life of the scope and
+// gives the caller's current device back when it ends.
+class DeviceScope {
+  public:
+    DeviceScope() = default;
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+    ~DeviceScope()
+    {
+        if (changed_)
+            cudaSetDevice(prev_);
+    }
+
+    fsdp_status enter(const void *p)
+    {
+        cudaPointerAttributes a;
+        cudaError_t err = cudaPointerGetAttributes(&a, p);
+        if (err != cudaSuccess)
+            return set_error(FSDP_ECUDA, "cudaPointerGetAttributes: %s", cudaGetErrorString(err));
+        if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+            return set_error(FSDP_EINVAL, "output buffer %p is not device memory", p);
+        if ((err = cudaGetDevice(&prev_)) != cudaSuccess)
+            return set_error(FSDP_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+        if (prev_ != a.device) {
+            if ((err = cudaSetDevice(a.device)) != cudaSuccess)
+                return set_error(FSDP_ECUDA, "cudaSetDevice: %s", cudaGetErrorString(err));
+            changed_ = true;
+        }
+        dev_ = a.device;
+        return FSDP_OK;
+    }
+    int device() const { return dev_; }
+
+  private:
+    int prev_ = -1, dev_ = -1;
+    bool changed_ = false;
+};
 
 // Persistent grid size for `kernel` on `dev`: resident CTAs per SM (at most
 // `max_per_sm`) x SMs.
@@ -699,13 +739,74 @@ fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const ch
     return check_launch(what);
 }
 
+// One kernel launch of a call over n units: its segments, and for each unit
+// slot k of the launch the caller's unit index units[k]. Slot k's rank r
+// buffer is entry k*R + r of the launch's pointer arrays (Seg::base = k*R).
+struct Launch {
+    const LaunchPlan *plan = nullptr;  // a layout's own plan (one unit), or
+    LaunchPlan merged;                 // segments merged from several units
+    std::vector<int> units;
+    const LaunchPlan &get() const { return plan ? *plan : merged; }
+};
+
+// The launches of a call over n layouts sharing R: consecutive units share
+// a launch while the launch holds at most kMaxSegsPerLaunch segments and
+// kMaxR pointers per array. One unit takes its layout's own plans.
+std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, bool padded)
+{
+    std::vector<Launch> out;
+    if (n == 1) {
+        for (const LaunchPlan &pl : padded ? Ls[0]->padded_plans : Ls[0]->valid_plans) {
+            out.emplace_back();
+            out.back().plan = &pl;
+            out.back().units.push_back(0);
+        }
+        return out;
+    }
+    const int R = Ls[0]->R;
+    const int max_units = kMaxR / R;
+    Launch cur;
+    for (int u = 0; u < n; u++) {
+        for (const LaunchPlan &pl : padded ? Ls[u]->padded_plans : Ls[u]->valid_plans) {
+            const bool has_slot = !cur.units.empty() && cur.units.back() == u;
+            if ((!has_slot && (int)cur.units.size() == max_units) ||
+                cur.merged.segs.size() + pl.segs.size() > (size_t)kMaxSegsPerLaunch) {
+                out.push_back(std::move(cur));
+                cur = Launch();
+            }
+            if (cur.units.empty() || cur.units.back() != u)
+                cur.units.push_back(u);
+            const int32_t base = (int32_t)(cur.units.size() - 1) * R;
+            for (Seg s : pl.segs) {
+                s.tile_begin += cur.merged.total_tiles;
+                s.base = base;
+                cur.merged.segs.push_back(s);
+            }
+            cur.merged.total_tiles += pl.total_tiles;
+        }
+    }
+    if (!cur.units.empty())
+        out.push_back(std::move(cur));
+    return out;
+}
+
+// Entry k*R + r of a launch's pointer array = the caller's entry u*R + r of
+// unit slot k's unit u (NULL when the caller passed no array).
+template <typename T, typename A>
+void bind(T *dst, A src, const Launch &l, int R)
+{
+    for (size_t k = 0; k < l.units.size(); k++)
+        for (int r = 0; r < R; r++)
+            dst[k * R + r] = src ? (T)src[(size_t)l.units[k] * R + r] : nullptr;
+}
+
 }  // namespace
 
 fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *param_shard,
                         float *const *master, void *stream)
 {
-    int dev;
-    fsdp_status st = select_device(master[0], &dev);
+    DeviceScope ds;
+    fsdp_status st = ds.enter(master[0]);
     if (st != FSDP_OK)
         return st;
     if (L->mode == FSDP_ZERO3) {
@@ -724,39 +825,39 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
     memset(&p, 0, sizeof p);
     p.full = full;
     p.R = L->R;
-    for (int r = 0; r < L->R; r++) {
-        p.master[r] = master[r];
-        p.pshard[r] = param_shard ? static_cast<uint16_t *>(param_shard[r]) : nullptr;
-    }
-    for (const LaunchPlan &plan : L->padded_plans) {
-        fill_segs(p, plan);
+    for (const Launch &l : plan_launches(1, &L, true)) {
+        bind(p.master, master, l, L->R);
+        bind(p.pshard, param_shard, l, L->R);
+        fill_segs(p, l.get());
         st = L->param_dtype == FSDP_BF16
-                 ? run(dev, pack_kernel<true>, p, (cudaStream_t)stream, "pack", kPackCtasPerSm)
-                 : run(dev, pack_kernel<false>, p, (cudaStream_t)stream, "pack", kPackCtasPerSm);
+                 ? run(ds.device(), pack_kernel<true>, p, (cudaStream_t)stream, "pack",
+                       kPackCtasPerSm)
+                 : run(ds.device(), pack_kernel<false>, p, (cudaStream_t)stream, "pack",
+                       kPackCtasPerSm);
         if (st != FSDP_OK)
             return st;
     }
     return FSDP_OK;
 }
 
-fsdp_status launch_all_gather(const fsdp_layout_t *L, const void *const *shard,
+fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void *const *shard,
                               void *const *full_out, void *stream)
 {
-    int dev;
-    fsdp_status st = select_device(full_out[0], &dev);
+    DeviceScope ds;
+    fsdp_status st = ds.enter(full_out[0]);
     if (st != FSDP_OK)
         return st;
+    const fsdp_layout_t *L = Ls[0];
+    const int dev = ds.device();
     GatherParams p;
     memset(&p, 0, sizeof p);
     p.R = L->R;
-    for (int r = 0; r < L->R; r++) {
-        p.shard[r] = static_cast<const unsigned char *>(shard[r]);
-        p.full[r] = static_cast<unsigned char *>(full_out[r]);
-    }
     cudaStream_t s = (cudaStream_t)stream;
     const bool bf16 = L->param_dtype == FSDP_BF16;
-    for (const LaunchPlan &plan : L->valid_plans) {
-        fill_segs(p, plan);
+    for (const Launch &l : plan_launches(n, Ls, false)) {
+        bind(p.shard, shard, l, L->R);
+        bind(p.full, full_out, l, L->R);
+        fill_segs(p, l.get());
         switch (bf16 ? L->R : -L->R) {
         case 2: st = run(dev, all_gather_kernel<2, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
         case 4: st = run(dev, all_gather_kernel<4, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
@@ -799,32 +900,33 @@ static fsdp_status rs_dispatch_dtypes(int dev, const fsdp_layout_t *L, RsParams 
     return rs_dispatch<false, false, kAccum>(dev, L->R, p, s);
 }
 
-fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, float *const *master,
-                            float *const *m, float *const *v, void *const *param_shard_out,
-                            float *const *grad_shard_out, const AdamScalars &c, void *stream,
-                            const float *const *acc)
+fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *const *grad,
+                            float *const *master, float *const *m, float *const *v,
+                            void *const *param_shard_out, float *const *grad_shard_out,
+                            const AdamScalars &c, void *stream, const float *const *acc)
 {
-    int dev;
-    fsdp_status st = select_device(master[0], &dev);
+    DeviceScope ds;
+    fsdp_status st = ds.enter(master[0]);
     if (st != FSDP_OK)
         return st;
+    const fsdp_layout_t *L = Ls[0];
+    const int R = L->R;
     RsParams p;
     memset(&p, 0, sizeof p);
-    p.R = L->R;
+    p.R = R;
     p.c = c;
-    for (int r = 0; r < L->R; r++) {
-        p.grad[r] = grad[r];
-        p.acc[r] = acc ? acc[r] : nullptr;
-        p.master[r] = master[r];
-        p.m[r] = m[r];
-        p.v[r] = v[r];
-        p.pshard[r] = param_shard_out ? static_cast<uint16_t *>(param_shard_out[r]) : nullptr;
-        p.gshard[r] = grad_shard_out ? grad_shard_out[r] : nullptr;
-    }
     cudaStream_t s = (cudaStream_t)stream;
-    for (const LaunchPlan &plan : L->valid_plans) {
-        fill_segs(p, plan);
-        st = acc ? rs_dispatch_dtypes<true>(dev, L, p, s) : rs_dispatch_dtypes<false>(dev, L, p, s);
+    for (const Launch &l : plan_launches(n, Ls, false)) {
+        bind(p.grad, grad, l, R);
+        bind(p.acc, acc, l, R);
+        bind(p.master, master, l, R);
+        bind(p.m, m, l, R);
+        bind(p.v, v, l, R);
+        bind(p.pshard, param_shard_out, l, R);
+        bind(p.gshard, grad_shard_out, l, R);
+        fill_segs(p, l.get());
+        st = acc ? rs_dispatch_dtypes<true>(ds.device(), L, p, s)
+                 : rs_dispatch_dtypes<false>(ds.device(), L, p, s);
         if (st != FSDP_OK)
             return st;
     }
@@ -834,8 +936,8 @@ fsdp_status launch_rs_adamw(const fsdp_layout_t *L, const void *const *grad, flo
 fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const void *const *grad,
                               int first, void *stream)
 {
-    int dev;
-    fsdp_status st = select_device(acc[0], &dev);
+    DeviceScope ds;
+    fsdp_status st = ds.enter(acc[0]);
     if (st != FSDP_OK)
         return st;
     AccumParams p;
@@ -851,13 +953,9 @@ fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const v
     }
     cudaStream_t s = (cudaStream_t)stream;
     if (L->grad_dtype == FSDP_BF16)
-        return run(dev, accumulate_kernel<true>, p, s, "accumulate", kAccumulateCtasPerSm);
-    return run(dev, accumulate_kernel<false>, p, s, "accumulate", kAccumulateCtasPerSm);
+        return run(ds.device(), accumulate_kernel<true>, p, s, "accumulate", kAccumulateCtasPerSm);
+    return run(ds.device(), accumulate_kernel<false>, p, s, "accumulate", kAccumulateCtasPerSm);
 }
-
-}  // namespace fsdp
-
-namespace fsdp {
 
 // The reduce-scatter + AdamW of unit A, then the gather of unit B, on one
 // stream. Single launches that interleave the two tile streams (tile by
@@ -871,16 +969,12 @@ fsdp_status launch_rs_adamw_gather(const fsdp_layout_t *A, const void *const *gr
                                    const AdamScalars &c, const fsdp_layout_t *B,
                                    const void *const *shard, void *const *full_out, void *stream)
 {
-    fsdp_status st = launch_rs_adamw(A, grad, master, m, v, param_shard_out, grad_shard_out, c,
-                                     stream);
+    fsdp_status st = launch_rs_adamw(1, &A, grad, master, m, v, param_shard_out, grad_shard_out,
+                                     c, stream, nullptr);
     if (st != FSDP_OK)
         return st;
-    return launch_all_gather(B, shard, full_out, stream);
+    return launch_all_gather(1, &B, shard, full_out, stream);
 }
-
-}  // namespace fsdp
-
-namespace fsdp {
 
 template <bool kGradBf16, bool kOutBf16>
 static fsdp_status ar_dispatch(int dev, int R, ReduceParams &p, cudaStream_t s)
@@ -897,8 +991,8 @@ static fsdp_status ar_dispatch(int dev, int R, ReduceParams &p, cudaStream_t s)
 fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, void *const *out,
                               fsdp_dtype out_dtype, void *stream)
 {
-    int dev;
-    fsdp_status st = select_device(out[0], &dev);
+    DeviceScope ds;
+    fsdp_status st = ds.enter(out[0]);
     if (st != FSDP_OK)
         return st;
     ReduceParams p;
@@ -913,6 +1007,7 @@ fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, v
     }
     cudaStream_t s = (cudaStream_t)stream;
     const bool gb = L->grad_dtype == FSDP_BF16, ob = out_dtype == FSDP_BF16;
+    const int dev = ds.device();
     if (gb && ob)
         return ar_dispatch<true, true>(dev, L->R, p, s);
     if (gb)

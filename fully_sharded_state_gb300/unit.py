@@ -79,27 +79,53 @@ class ShardedUnit:
     def all_gather(self, full_out, stream=None) -> None:
         capi.fsdp_all_gather_unflatten(self.layout, self.gather_sources(), full_out, stream)
 
+    def _next_step(self, step):
+        return self.step + 1 if step is None else int(step)
+
     def reduce_scatter_adamw(self, grads, hp: capi.AdamWHP, grad_shard_out=None,
                              step: int | None = None, stream=None) -> None:
-        """One optimizer step from the R ranks' full local gradients."""
-        self.step = self.step + 1 if step is None else int(step)
+        """One optimizer step from the R ranks' full local gradients. The
+        step count advances only when the call is accepted."""
+        t = self._next_step(step)
         capi.fsdp_reduce_scatter_adamw(self.layout, grads, self.master, self.m, self.v,
-                                       self.param_shard, grad_shard_out, hp, self.step, stream)
+                                       self.param_shard, grad_shard_out, hp, t, stream)
+        self.step = t
 
     def reduce_scatter_adamw_and_gather(self, grads, hp: capi.AdamWHP, other: "ShardedUnit",
                                         other_full, grad_shard_out=None, step: int | None = None,
                                         stream=None) -> None:
         """This unit's optimizer step, then the all-gather of `other` (a different
         unit, e.g. the next one to be computed), validated together."""
-        self.step = self.step + 1 if step is None else int(step)
+        t = self._next_step(step)
         capi.fsdp_reduce_scatter_adamw_gather(
             self.layout, grads, self.master, self.m, self.v, self.param_shard, grad_shard_out,
-            hp, self.step, other.layout, other.gather_sources(), other_full, stream)
+            hp, t, other.layout, other.gather_sources(), other_full, stream)
+        self.step = t
 
     def all_reduce(self, grads, out, out_dtype: str = "f32", stream=None) -> None:
         """DDP's all-reduce of the R full gradients into R full outputs
         (fp32 or bf16), for comparison with the sharded path."""
         capi.fsdp_all_reduce(self.layout, grads, out, _DT[out_dtype][0], stream)
+
+    # -- prepared calls (checked once, re-issued every step) -----------------
+    def prepare_all_gather(self, full_out):
+        """The all-gather into ``full_out`` with its arguments bound; call the
+        result (optionally with ``stream=``) to issue it."""
+        return capi.prepare_fsdp_all_gather_unflatten(self.layout, self.gather_sources(),
+                                                      full_out)
+
+    def prepare_reduce_scatter_adamw(self, grads, grad_shard_out=None):
+        """The reduce-scatter + AdamW step on ``grads`` with its arguments
+        bound. Call the result with ``hp`` (and ``step=``, ``stream=``); the
+        step count advances as with reduce_scatter_adamw."""
+        call = capi.prepare_fsdp_reduce_scatter_adamw(self.layout, grads, self.master, self.m,
+                                                      self.v, self.param_shard, grad_shard_out)
+
+        def run(hp: capi.AdamWHP, step: int | None = None, stream=None) -> None:
+            t = self._next_step(step)
+            call(hp, t, stream)
+            self.step = t
+        return run
 
     # -- gradient accumulation over micro-batches ---------------------------
     def alloc_accumulators(self):
@@ -114,7 +140,55 @@ class ShardedUnit:
     def reduce_scatter_adamw_accum(self, acc, grads, hp: capi.AdamWHP, grad_shard_out=None,
                                    step: int | None = None, stream=None) -> None:
         """The optimizer step on acc + grads (the last micro-batch fused in)."""
-        self.step = self.step + 1 if step is None else int(step)
+        t = self._next_step(step)
         capi.fsdp_reduce_scatter_adamw_accum(self.layout, acc, grads, self.master, self.m,
-                                             self.v, self.param_shard, grad_shard_out, hp,
-                                             self.step, stream)
+                                             self.v, self.param_shard, grad_shard_out, hp, t,
+                                             stream)
+        self.step = t
+
+
+# -- several units per launch --------------------------------------------------
+
+def all_gather_units(units, full_outs, stream=None) -> None:
+    """The all-gather + unflatten of every unit in ``units`` (same R and
+    dtypes) in one launch; ``full_outs[u]`` is unit u's list of R outputs."""
+    capi.fsdp_all_gather_unflatten_units([U.layout for U in units],
+                                         [U.gather_sources() for U in units], full_outs, stream)
+
+
+def reduce_scatter_adamw_units(units, grads, hp: capi.AdamWHP, grad_shard_outs=None,
+                               step: int | None = None, stream=None) -> None:
+    """One optimizer step of every unit in ``units`` in one launch. All units
+    take the same step count: one past the first unit's, or ``step``."""
+    t = units[0]._next_step(step)
+    bf16 = units[0].param_shard is not None
+    capi.fsdp_reduce_scatter_adamw_units(
+        [U.layout for U in units], grads, [U.master for U in units], [U.m for U in units],
+        [U.v for U in units], [U.param_shard for U in units] if bf16 else None,
+        grad_shard_outs, hp, t, stream)
+    for U in units:
+        U.step = t
+
+
+
+def prepare_all_gather_units(units, full_outs):
+    """all_gather_units with its arguments bound once (see PreparedCall)."""
+    return capi.prepare_fsdp_all_gather_unflatten_units([U.layout for U in units],
+                                                        [U.gather_sources() for U in units],
+                                                        full_outs)
+
+
+def prepare_reduce_scatter_adamw_units(units, grads, grad_shard_outs=None):
+    """reduce_scatter_adamw_units with its arguments bound once; call the
+    result with ``hp`` (and ``step=``, ``stream=``)."""
+    bf16 = units[0].param_shard is not None
+    call = capi.prepare_fsdp_reduce_scatter_adamw_units(
+        [U.layout for U in units], grads, [U.master for U in units], [U.m for U in units],
+        [U.v for U in units], [U.param_shard for U in units] if bf16 else None, grad_shard_outs)
+
+    def run(hp: capi.AdamWHP, step: int | None = None, stream=None) -> None:
+        t = units[0]._next_step(step)
+        call(hp, t, stream)
+        for U in units:
+            U.step = t
+    return run

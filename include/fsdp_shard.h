@@ -31,12 +31,23 @@
  *                              FSDPAdamW; walkthrough Step 6).
  *
  * Conventions (all entry points):
- *  - Every call is host-validated first. An argument error returns a
- *    negative status, sets the thread's fsdp_last_error() message and
- *    launches nothing. No kernel traps or asserts.
+ *  - Every call checks its arguments on the host before it launches
+ *    anything: the layout and hyper-parameters, every pointer array and
+ *    every pointer in it (non-NULL, 16-byte aligned), and that no output
+ *    range [p, p + bytes) overlaps any other buffer's range, where bytes is
+ *    what the layout says the buffer holds (e.g. P elements of grad_dtype
+ *    for a full gradient). It also checks that the first output buffer is
+ *    device memory. A failed check returns a negative status, sets the
+ *    thread's fsdp_last_error() message and launches nothing. A plain
+ *    pointer carries no size, dtype or device, so the library cannot see
+ *    that an allocation is too short, holds another dtype or lives on
+ *    another GPU: that is the caller's part (the Python binding checks it
+ *    on every tensor before the call). No kernel traps or asserts.
  *  - Kernel calls are asynchronous on `stream` (a cudaStream_t; NULL is the
- *    legacy default stream) and never synchronise. The device is the one that
- *    owns the first output buffer.
+ *    legacy default stream) and never synchronise. They run on the device
+ *    that owns the first output buffer, which every buffer of the call must
+ *    be on; the calling thread's current device is the same after the call
+ *    as before it.
  *  - Buffer arguments are host arrays of R device pointers, one per virtual
  *    rank, indexed by rank. The caller owns all device memory and the
  *    stream; the library owns only the opaque layout (host memory).
@@ -223,6 +234,40 @@ fsdp_status fsdp_accumulate_grad(const fsdp_layout_t *layout, float *const *acc_
  * Errors as fsdp_reduce_scatter_adamw. */
 fsdp_status fsdp_reduce_scatter_adamw_accum(const fsdp_layout_t *layout,
                                             const float *const *acc_full,
+                                            const void *const *grad_full, float *const *master,
+                                            float *const *m, float *const *v,
+                                            void *const *param_shard_out,
+                                            float *const *grad_shard_out, const fsdp_adamw_hp *hp,
+                                            int64_t step, void *stream);
+
+/* Several units in one call: the all-gather + unflatten of n_units units,
+ * each exactly as fsdp_all_gather_unflatten would do it, issued as one
+ * kernel launch (or a few, past 256 parameters or 64 per-rank pointers per
+ * launch). This is the pages' bucketing taken one level up: many small
+ * collectives fused into one ("从源码理解 FSDP", §5.3 bucketing small tensors
+ * into one communication; "FSDP2 的参数全聚合、梯度归约分片与显存峰值", §05
+ * how grouping sets the size of each all-gather). It exists for small units,
+ * whose per-call host work and per-launch ramp dominate their streaming time.
+ * layouts[u]: unit u's layout; all share R and the dtypes (else FSDP_EINVAL);
+ * one layout may serve several units. shard and full_out hold n_units*R
+ * device pointers, unit-major: entry u*R + r is unit u's rank r. Every buffer
+ * is validated as in the one-unit call, and outputs must not overlap any
+ * buffer of any unit. Units with no elements are skipped (their pointers may
+ * be NULL). Errors: as fsdp_all_gather_unflatten, plus FSDP_EINVAL for
+ * n_units < 1 or a NULL layout. */
+fsdp_status fsdp_all_gather_unflatten_units(int n_units, const fsdp_layout_t *const *layouts,
+                                            const void *const *shard, void *const *full_out,
+                                            void *stream);
+
+/* The reduce-scatter + AdamW step of n_units units in one call (see
+ * fsdp_all_gather_unflatten_units for the grouping and the pointer arrays,
+ * which here are grad_full, master, m, v, param_shard_out and, if not NULL,
+ * grad_shard_out, each n_units*R entries, unit-major). Every unit takes the
+ * same hyper-parameters and step, and gets exactly the result of
+ * fsdp_reduce_scatter_adamw. param_shard_out is required for BF16 layouts and
+ * must be NULL for F32 layouts. Errors: as fsdp_reduce_scatter_adamw, plus
+ * FSDP_EINVAL for n_units < 1 or a NULL layout. */
+fsdp_status fsdp_reduce_scatter_adamw_units(int n_units, const fsdp_layout_t *const *layouts,
                                             const void *const *grad_full, float *const *master,
                                             float *const *m, float *const *v,
                                             void *const *param_shard_out,

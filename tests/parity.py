@@ -269,3 +269,51 @@ def run_accumulation_case(case: UnitCase, K: int):
             assert torch.equal(gsh[r].view(torch.int32), gsh2[r].view(torch.int32))
             assert torch.equal(U.master[r].view(torch.int32), F.master[r].view(torch.int32))
     torch.cuda.synchronize()
+
+
+def run_units_case(cases, step: int = 1, share_layout: bool = False):
+    """Several units through the multi-unit calls (one launch where they fit):
+    all-gather + unflatten of every unit, then reduce-scatter + AdamW of every
+    unit, each unit compared with the oracle on its own inputs."""
+    from fully_sharded_state_gb300 import all_gather_units, reduce_scatter_adamw_units
+    c0 = cases[0]
+    bf16 = c0.param_dtype == "bf16"
+    units, Os, ws, gs = [], [], [], []
+    for c in cases:
+        w, grads = host_inputs(c)
+        U = ShardedUnit(c.shapes, c.R, c.mode, c.param_dtype, c.grad_dtype)
+        if share_layout and units:
+            U.layout = units[0].layout  # one layout object serving several units
+        U.shard_from_full(to_dev(w))
+        units.append(U)
+        Os.append(oracle.layout(omode(c.mode), c.R, c.shapes))
+        ws.append(w)
+        gs.append(grads)
+    fulls = [U.alloc_full() for U in units]
+    all_gather_units(units, fulls)
+    packed = [oracle.pack(O, w, with_bf16=bf16) for O, w in zip(Os, ws)]
+    for u, (O, (masters, p16)) in enumerate(zip(Os, packed)):
+        want = oracle.all_gather(O, p16 if bf16 else masters)
+        for d in range(c0.R):
+            assert_bits_equal(host(fulls[u][d]), want[d], f"unit {u} full[{d}]")
+    lr, b1, b2, eps, wd = c0.hp
+    gsh = [[torch.zeros(U.S, dtype=torch.float32, device="cuda") for _ in range(c0.R)]
+           for U in units]
+    reduce_scatter_adamw_units(units, [[to_dev(g) for g in grads] for grads in gs],
+                               AdamWHP(lr, b1, b2, eps, wd), grad_shard_outs=gsh, step=step)
+    for u, (U, O, (masters, _)) in enumerate(zip(units, Os, packed)):
+        m = [np.zeros(U.S, np.float32) for _ in range(c0.R)]
+        v = [np.zeros(U.S, np.float32) for _ in range(c0.R)]
+        want_g, want_p16 = oracle.rs_adamw(O, gs[u], masters, m, v,
+                                           oracle.AdamWHP(lr, b1, b2, eps, wd), step,
+                                           with_bf16=bf16)
+        assert U.step == step
+        for r in range(c0.R):
+            assert_bits_equal(host(gsh[u][r]), want_g[r], f"unit {u} reduce-scatter[{r}]")
+            assert_master_close(host(U.master[r]), masters[r], f"unit {u} master[{r}]")
+            assert_moment_close(host(U.m[r]), m[r], f"unit {u} m[{r}]")
+            assert_moment_close(host(U.v[r]), v[r], f"unit {u} v[{r}]")
+            if bf16:
+                assert_bf16_close(host(U.param_shard[r]), want_p16[r], f"unit {u} bf16[{r}]")
+    torch.cuda.synchronize()
+    return units

@@ -298,3 +298,160 @@ def test_accumulation_rejects_bad_arguments(lib):
                                              a["v"], a["pshard"], None, ctypes.byref(a["hp"]),
                                              0, None)
     assert st == capi.FSDP_EINVAL
+
+
+# ---- the binding's checks of tensor arguments (tensor metadata only) -------
+
+class FakeTensor:
+    """Metadata of a CUDA tensor, enough for the binding's checks; its data
+    pointer is never dereferenced because every case below is rejected."""
+
+    def __init__(self, numel, dtype, device="cuda:0", contiguous=True, cuda=True):
+        import torch
+        self._n, self.dtype, self.device = numel, dtype, torch.device(device)
+        self._c, self.is_cuda = contiguous, cuda
+
+    def numel(self):
+        return self._n
+
+    def is_contiguous(self):
+        return self._c
+
+    def data_ptr(self):
+        return BASE
+
+
+def _binding_case(**over):
+    torch = pytest.importorskip("torch")
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(64, 8)], capi.FSDP_BF16, capi.FSDP_BF16)
+    P, S = L.full_numel, L.shard_numel
+    args = dict(shard=[FakeTensor(S, torch.bfloat16) for _ in range(2)],
+                full_out=[FakeTensor(P, torch.bfloat16) for _ in range(2)])
+    args.update({k: v(torch, P, S) for k, v in over.items()})
+    return L, args
+
+
+@pytest.mark.parametrize("over,needle", [
+    (dict(full_out=lambda t, P, S: [FakeTensor(P - 1, t.bfloat16), FakeTensor(P, t.bfloat16)]),
+     "elements"),
+    (dict(shard=lambda t, P, S: [FakeTensor(S, t.bfloat16), FakeTensor(S - 8, t.bfloat16)]),
+     "elements"),
+    (dict(full_out=lambda t, P, S: [FakeTensor(P, t.float32), FakeTensor(P, t.bfloat16)]),
+     "dtype"),
+    (dict(shard=lambda t, P, S: [FakeTensor(S, t.bfloat16, "cuda:1"),
+                                 FakeTensor(S, t.bfloat16)]), "is on"),
+    (dict(shard=lambda t, P, S: [FakeTensor(S, t.bfloat16, contiguous=False),
+                                 FakeTensor(S, t.bfloat16)]), "contiguous"),
+    (dict(shard=lambda t, P, S: [FakeTensor(S, t.bfloat16)]), "expected 2"),
+    (dict(shard=lambda t, P, S: [FakeTensor(S, t.bfloat16, "cpu", cuda=False),
+                                 FakeTensor(S, t.bfloat16)]), "not a CUDA tensor"),
+])
+def test_binding_checks_tensor_size_dtype_device(lib, over, needle):
+    L, a = _binding_case(**over)
+    with pytest.raises(capi.FsdpArgumentError) as e:
+        capi.fsdp_all_gather_unflatten(L, a["shard"], a["full_out"])
+    assert e.value.status == capi.FSDP_EINVAL and needle in str(e.value)
+
+
+def test_binding_checks_reduce_scatter_state_dtypes(lib):
+    torch = pytest.importorskip("torch")
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(64, 8)], capi.FSDP_BF16, capi.FSDP_BF16)
+    P, S = L.full_numel, L.shard_numel
+    f32 = lambda n: [FakeTensor(n, torch.float32) for _ in range(2)]
+    b16 = lambda n: [FakeTensor(n, torch.bfloat16) for _ in range(2)]
+    hp = _hp()
+    # fp32 gradients for a bf16-gradient layout
+    with pytest.raises(capi.FsdpArgumentError, match="grad_full"):
+        capi.fsdp_reduce_scatter_adamw(L, f32(P), f32(S), f32(S), f32(S), b16(S), None, hp, 1)
+    # bf16 master
+    with pytest.raises(capi.FsdpArgumentError, match="master"):
+        capi.fsdp_reduce_scatter_adamw(L, b16(P), b16(S), f32(S), f32(S), b16(S), None, hp, 1)
+    # a short second moment
+    with pytest.raises(capi.FsdpArgumentError, match=r"v\[1\]"):
+        capi.fsdp_reduce_scatter_adamw(L, b16(P), f32(S), f32(S), [f32(S)[0], f32(S - 1)[0]],
+                                       b16(S), None, hp, 1)
+    # accumulators must be fp32 and full-unit sized
+    with pytest.raises(capi.FsdpArgumentError, match="acc_full"):
+        capi.fsdp_reduce_scatter_adamw_accum(L, f32(P - 8), b16(P), f32(S), f32(S), f32(S),
+                                             b16(S), None, hp, 1)
+    with pytest.raises(capi.FsdpArgumentError, match="out"):
+        capi.fsdp_all_reduce(L, b16(P), b16(P - 1), capi.FSDP_BF16)
+
+
+def test_unit_step_advances_only_on_accepted_calls(lib):
+    torch = pytest.importorskip("torch")
+    from fully_sharded_state_gb300 import unit as unit_mod
+
+    class Stub(unit_mod.ShardedUnit):
+        def __init__(self):  # no device buffers: only the step bookkeeping is exercised
+            self.layout = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(64, 8)], capi.FSDP_BF16,
+                                           capi.FSDP_BF16)
+            S = self.layout.shard_numel
+            self.master = self.m = self.v = [FakeTensor(S, torch.float32) for _ in range(2)]
+            self.param_shard = [FakeTensor(S, torch.bfloat16) for _ in range(2)]
+            self.step = 4
+
+    U = Stub()
+    short = [FakeTensor(1, torch.bfloat16) for _ in range(2)]
+    with pytest.raises(capi.FsdpArgumentError):
+        U.reduce_scatter_adamw(short, _hp())
+    assert U.step == 4
+    with pytest.raises(capi.FsdpArgumentError):
+        U.reduce_scatter_adamw_accum(short, short, _hp())
+    assert U.step == 4
+
+
+# ---- several units per call --------------------------------------------------
+
+def _units_rs(lib, layouts, R, over=None, bytes_per=1 << 22):
+    n = len(layouts)
+    k = iter(range(10_000))
+    arr = lambda: _ptrs([BASE + next(k) * bytes_per for _ in range(n * R)])
+    a = dict(grad=arr(), master=arr(), m=arr(), v=arr(), pshard=arr(), gshard=None, hp=_hp(),
+             step=1)
+    a.update(over or {})
+    lay = _ptrs([L.handle for L in layouts])
+    return lib.fsdp_reduce_scatter_adamw_units(n, lay, a["grad"], a["master"], a["m"], a["v"],
+                                               a["pshard"], a["gshard"], ctypes.byref(a["hp"]),
+                                               a["step"], None)
+
+
+def test_units_calls_reject_bad_arguments(lib):
+    A = capi.fsdp_layout(capi.FSDP_FLAT, 4, [(512, 512)], capi.FSDP_BF16, capi.FSDP_BF16)
+    B8 = capi.fsdp_layout(capi.FSDP_FLAT, 8, [(512, 512)], capi.FSDP_BF16, capi.FSDP_BF16)
+    F = capi.fsdp_layout(capi.FSDP_FLAT, 4, [(512, 512)], capi.FSDP_F32, capi.FSDP_BF16)
+    MB = 1 << 22
+    sh = _ptrs([BASE + k * MB for k in range(8)])
+    fo = _ptrs([BASE + (100 + k) * MB for k in range(8)])
+    g = lambda *Ls: _ptrs([L.handle for L in Ls])
+    assert lib.fsdp_all_gather_unflatten_units(0, g(A), sh, fo, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_all_gather_unflatten_units(2, None, sh, fo, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_all_gather_unflatten_units(2, _ptrs([A.handle, 0]), sh, fo,
+                                               None) == capi.FSDP_EINVAL
+    # mixed R or dtypes
+    assert lib.fsdp_all_gather_unflatten_units(2, g(A, B8), sh, fo, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_all_gather_unflatten_units(2, g(A, F), sh, fo, None) == capi.FSDP_EINVAL
+    # unit 1's destination 2 (entry 6) overlaps unit 0's destination 0
+    bad = _ptrs([BASE + (100 + k) * MB for k in range(6)] + [BASE + 100 * MB + 64,
+                                                            BASE + 200 * MB])
+    assert lib.fsdp_all_gather_unflatten_units(2, g(A, A), sh, bad, None) == capi.FSDP_EINVAL
+    assert b"full_out" in lib.fsdp_last_error()
+    # a misaligned pointer is reported by its index in the whole array
+    bad = _ptrs([BASE + (100 + k) * MB for k in range(5)] + [BASE + 300 * MB + 2,
+                                                            BASE + 301 * MB, BASE + 302 * MB])
+    assert lib.fsdp_all_gather_unflatten_units(2, g(A, A), sh, bad, None) == capi.FSDP_EALIGN
+    assert b"full_out[5]" in lib.fsdp_last_error()
+    # the reduce-scatter: bf16 layouts need param_shard_out; F32 layouts take none
+    assert _units_rs(lib, [A, A], 4, dict(pshard=None)) == capi.FSDP_EINVAL
+    assert _units_rs(lib, [F, F], 4) == capi.FSDP_EINVAL
+    assert _units_rs(lib, [A, A], 4, dict(step=0)) == capi.FSDP_EINVAL
+    assert _units_rs(lib, [A, B8], 4) == capi.FSDP_EINVAL
+
+
+def test_units_calls_skip_empty_units(lib):
+    E = capi.fsdp_layout(capi.FSDP_PER_PARAM, 4, [(0, 8)], capi.FSDP_BF16, capi.FSDP_BF16)
+    nul = _ptrs([0] * 8)
+    lay = _ptrs([E.handle, E.handle])
+    assert lib.fsdp_all_gather_unflatten_units(2, lay, nul, nul, None) == capi.FSDP_OK
+    assert lib.fsdp_reduce_scatter_adamw_units(2, lay, nul, nul, nul, nul, nul, None,
+                                               ctypes.byref(_hp()), 1, None) == capi.FSDP_OK

@@ -156,3 +156,74 @@ def test_unit_past_two_to_the_31_elements(cuda_lib):
     assert_moment_close(_at(U.v, rank, idx, dev), v_o, "v")
     assert_bf16_close(_at(U.param_shard, rank, idx, dev), oracle.f32_to_bf16(w_o))
     torch.cuda.synchronize()
+
+
+def test_llama_unit_whole_vs_oracle(cuda_lib):
+    """One whole Llama-style unit (218,112,000 parameters, R = 8, bf16
+    parameters and gradients) through the calls the benchmark times, every
+    output element compared with the oracle on the same host-generated
+    inputs: pack (bit-exact), all 8 gather destinations (bit-exact), the fp32
+    reduce-scatter shard (bit-exact), master/m/v after a step-3 update from
+    prior moments (1e-5 bounds), the bf16 shard (1 ulp), and the gather of
+    the updated shards."""
+    wl = synth.WORKLOADS["llama4"]
+    u = 1
+    shapes = wl.unit_shapes(u)
+    R = wl.R
+    dev = torch.device("cuda")
+    O = oracle.layout(oracle.PER_PARAM, R, shapes)
+    U = ShardedUnit(shapes, R, "per_param", "bf16", "bf16", names=[n for n, _ in wl.units[u]])
+    assert (U.P, U.S) == (O.full_numel, O.shard_numel) == (218_112_000, 27_264_000)
+
+    # a2: shard from full
+    w = synth.host_weights(wl, u)
+    U.shard_from_full(torch.from_numpy(w).to(dev))
+    masters, p16 = oracle.pack(O, w, with_bf16=True)
+    del w
+    for r in range(R):
+        assert_bits_equal(host(U.master[r]), masters[r], f"pack master[{r}]")
+        assert_bits_equal(host(U.param_shard[r]), p16[r], f"pack bf16[{r}]")
+
+    # a3: all-gather + unflatten, every destination, every element
+    full = U.alloc_full()
+    U.all_gather(full)
+    want = oracle.all_gather(O, p16)
+    for d in range(R):
+        assert_bits_equal(host(full[d]), want[d], f"all-gather full[{d}]")
+    del want
+
+    # a4-a6: reduce-scatter + AdamW at step 3 from prior moments
+    ms, vs = synth.host_moments(wl, u, U.S)
+    for r in range(R):
+        U.m[r].copy_(torch.from_numpy(ms[r]))
+        U.v[r].copy_(torch.from_numpy(vs[r]))
+    grads = synth.host_grads(wl, u)
+    gdev = [torch.from_numpy(g.view(np.int16)).to(dev).view(torch.bfloat16) for g in grads]
+    gsh = [torch.empty(U.S, dtype=torch.float32, device=dev) for _ in range(R)]
+    hp = AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
+    U.reduce_scatter_adamw(gdev, hp, grad_shard_out=gsh, step=3)
+    del gdev
+    want_g, want_p16 = oracle.rs_adamw(O, grads, masters, ms, vs,
+                                       oracle.AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps,
+                                                      wl.weight_decay), 3, with_bf16=True)
+    del grads
+    for r in range(R):
+        n = O.rank_numel(r)  # the reduce-scatter writes owned elements only
+        got_g = host(gsh[r])
+        for i in range(len(shapes)):
+            s, c = O.rank_rows(i, r)
+            a = int(O.shard_off[i])
+            b = a + c * int(O.inner[i])
+            assert_bits_equal(got_g[a:b], want_g[r][a:b], f"reduce-scatter shard[{r}] param {i}")
+        assert n > 0
+        assert_master_close(host(U.master[r]), masters[r], f"master[{r}]")
+        assert_moment_close(host(U.m[r]), ms[r], f"m[{r}]")
+        assert_moment_close(host(U.v[r]), vs[r], f"v[{r}]")
+        assert_bf16_close(host(U.param_shard[r]), want_p16[r], f"bf16 shard[{r}]")
+
+    # the gather of the updated shards
+    U.all_gather(full)
+    want = oracle.all_gather(O, want_p16)
+    for d in range(R):
+        assert_bf16_close(host(full[d]), want[d], f"gather after the step full[{d}]")
+    torch.cuda.synchronize()
