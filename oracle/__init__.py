@@ -37,17 +37,24 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _vpp = ctypes.POINTER(ctypes.c_void_p)
 
 
-def build(force: bool = False) -> str:
-    """Compile the C oracle into ``oracle/libfsdp_oracle.so`` (gcc, no contraction)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+_OMP_LIB_PATH = os.path.join(_HERE, "libfsdp_oracle_omp.so")
+
+
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile the C oracle into ``oracle/libfsdp_oracle.so`` (gcc, no
+    contraction), or with ``openmp`` the same source with -fopenmp into
+    ``oracle/libfsdp_oracle_omp.so`` (element loops split over threads,
+    per-element arithmetic unchanged)."""
+    path = _OMP_LIB_PATH if openmp else _LIB_PATH
+    if (not force and os.path.exists(path)
+            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+           *(["-fopenmp"] if openmp else []), "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 def _load(path: str):
@@ -107,10 +114,25 @@ def lib():
 
 def use_library(path: str) -> None:
     """Point this module at another build of the oracle source for the rest of
-    the process. Used only by the tests that plant a mistake in a copy of the
-    oracle and check that the pins catch it."""
+    the process: a copy with a planted mistake (the tests that check the pins
+    catch it), or the OpenMP build (the timed CPU baseline)."""
     global _lib
     _lib = _load(path)
+
+
+class using:
+    """Context manager: the oracle functions use the library at ``path``
+    inside the block and the plain build after it."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        use_library(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        use_library(build())
 
 
 def _i64(values) -> np.ndarray:

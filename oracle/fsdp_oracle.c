@@ -10,6 +10,12 @@
  * Every float operation below is a single IEEE-754 binary32 operation rounded
  * to nearest even; nothing is contracted into an FMA or reassociated.
  *
+ * The same source also builds with -fopenmp into a second library that the
+ * CPU baseline times on all host cores. The only OpenMP directives split
+ * element loops (and the gather's destinations) over threads: each element's
+ * arithmetic and its order of operations are those of the plain build, so
+ * both builds give identical bits. The plain build ignores the directives.
+ *
  * Sources (web pages on FSDP):
  *  [Walkthrough]   "FSDP Training Step Walkthrough": Setup, Initial state,
  *                  Step 1.1 All-Gather, Step 4.4 Reduce-Scatter, Step 6
@@ -201,6 +207,7 @@ uint16_t orc_f32_to_bf16(float f)
 
 void orc_f32_to_bf16_array(int64_t count, const float *x, uint16_t *y)
 {
+#pragma omp parallel for schedule(static) if (count > 65536)
     for (int64_t k = 0; k < count; k++)
         y[k] = orc_f32_to_bf16(x[k]);
 }
@@ -272,6 +279,7 @@ int orc_all_gather(int mode, int64_t R, int64_t n, const int64_t *d0, const int6
     if (mode == ORC_ZERO3)
         orc_zero3_owners(R, n, d0, inner, owner);
     int64_t P = out[0], S = out[1];
+#pragma omp parallel for schedule(static) if (P > 65536)
     for (int64_t d = 0; d < R; d++) {
         char *dst = (char *)full[d];
         if (mode != ORC_FLAT) {
@@ -311,6 +319,7 @@ int orc_all_gather(int mode, int64_t R, int64_t n, const int64_t *d0, const int6
 void orc_sum_ranks(int64_t R, int64_t count, int dtype, const void *const *g, float *out)
 {
     float inv_R = 1.0f / (float)R;
+#pragma omp parallel for schedule(static) if (count > 65536)
     for (int64_t k = 0; k < count; k++) {
         float acc = load_as_f32(g[0], dtype, k);
         for (int64_t q = 1; q < R; q++)
@@ -339,6 +348,7 @@ int orc_reduce_scatter(int mode, int64_t R, int64_t n, const int64_t *d0, const 
     int64_t esize = grad_dtype == ORC_BF16 ? 2 : 4;
     const void *ptrs[R];
     for (int64_t r = 0; r < R; r++) {
+#pragma omp parallel for schedule(static) if (S > 65536)
         for (int64_t k = 0; k < S; k++)
             gshard[r][k] = 0.0f;
         if (mode != ORC_FLAT) {
@@ -384,6 +394,7 @@ void orc_adamw(int64_t count, const float *g, float *w, float *m, float *v,
     float step_size = (float)(lr / (1.0 - pow(beta1, (double)t)));
     float bc2_sqrt = (float)sqrt(1.0 - pow(beta2, (double)t));
     float epsf = (float)eps;
+#pragma omp parallel for schedule(static) if (count > 65536)
     for (int64_t k = 0; k < count; k++) {
         float gk = g[k];
         float wk = w[k] * decay;
