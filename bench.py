@@ -16,6 +16,7 @@ step, in GB/s, summed over GPUs (replicas) for N > 1.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama4|llama_attn] [--no-e2e] [--no-cpu-baseline]
+                    [--no-configs] [--no-memory] [--no-ceilings]
 """
 from __future__ import annotations
 
@@ -248,15 +249,55 @@ def host_cpu() -> str:
     return "unknown"
 
 
-def cpu_baseline(wl, target_s: float = 10.0):
-    smp = OracleSample(wl)
-    dt = smp.run()
-    reps = max(1, min(30, int(target_s / max(dt, 1e-3))))
-    total_t = dt + sum(smp.run() for _ in range(reps - 1))
-    return {"value": round(reps * smp.nbytes / total_t / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle", "sample": f"{reps} runs of {smp.desc}",
-            "seconds": round(total_t, 2), "host_cores_available": os.cpu_count(),
-            "host_cpu": host_cpu()}
+def cpu_baseline(wl, shapes, w_dev, grads_dev):
+    """The CPU oracle timed on one whole unit of the GPU arm's own inputs (its
+    device-generated weights and R gradients, copied to the host): once with
+    the plain single-thread build, then with the OpenMP build of the same
+    source on all host cores, whose outputs must be bit-identical."""
+    import oracle
+    R = wl.R
+    O = oracle.layout(oracle.PER_PARAM, R, shapes)
+    P, S = O.full_numel, O.shard_numel
+    w = w_dev.detach().cpu().numpy()
+    grads = [g.detach().view(torch_int16()).cpu().numpy().view(np.uint16) for g in grads_dev]
+    hp = oracle.AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
+    masters0, p16_0 = oracle.pack(O, w, with_bf16=True)
+    del w
+    nbytes = all_gather_bytes(P, R) + rs_adamw_bytes(P, R)
+
+    def one_run():
+        masters = [x.copy() for x in masters0]
+        m = [np.zeros(S, np.float32) for _ in range(R)]
+        v = [np.zeros(S, np.float32) for _ in range(R)]
+        t0 = time.perf_counter()
+        full = oracle.all_gather(O, p16_0)
+        _, p16 = oracle.rs_adamw(O, grads, masters, m, v, hp, 1, with_bf16=True)
+        dt = time.perf_counter() - t0
+        return dt, full, masters, m, v, p16
+
+    dt1, *single = one_run()
+    with oracle.using(oracle.build(openmp=True)):
+        runs = [one_run() for _ in range(3)]
+    dt_omp = statistics.median(r[0] for r in runs)
+    omp = runs[-1][1:]
+    identical = all(np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
+                    for xs, ys in zip(single, omp) for a, b in zip(xs, ys))
+    cores = os.cpu_count()
+    desc = (f"one whole unit of the benchmark ({P:,} params, R={R}) on the GPU arm's own "
+            "inputs: oracle all-gather + reduce-scatter/AdamW")
+    return {"value": round(nbytes / dt1 / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": desc + ", single thread", "seconds": round(dt1, 3),
+            "openmp": {"value": round(nbytes / dt_omp / 1e9, 4), "unit": UNIT, "cores": cores,
+                       "seconds_median_of_3": round(dt_omp, 3),
+                       "bit_identical_to_single_thread": bool(identical),
+                       "build": "same oracle source, gcc -fopenmp (element loops split over "
+                                "threads)"},
+            "host_cores_available": cores, "host_cpu": host_cpu()}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
 
 
 def run_reference(args):
@@ -285,6 +326,238 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm --
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
+def roofline_entry(kernel, nbytes, ms, peak, peak_src, traffic=None, ceilings=None):
+    """Roofline record of one kernel: algorithmic bytes per launch over its
+    mean CUDA-event launch time, as a fraction of the measured HBM copy peak,
+    of the nominal HBM bandwidth and (when measured in the run) of the
+    write-only stream ceiling."""
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    e = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+         "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": peak_src,
+         "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+         "nominal_peak": NOMINAL_HBM_GBS, "algorithmic_bytes_per_launch": int(nbytes),
+         "avg_launch_ms": round(ms, 4), "traffic": traffic}
+    if ceilings and ceilings.get("write_only_x_R_gbs"):
+        e["frac_of_write_ceiling"] = round(gbs / ceilings["write_only_x_R_gbs"], 4)
+    return e
+
+
+def timed_back_to_back(torch, stream, fn, n=50, warm=5):
+    """CUDA-event time (ms) per call of fn() issued n times back to back on
+    `stream` (throughput: the host issues ahead while the GPU works)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def timed_launches(torch, stream, fn, n=20, warm=3):
+    """Mean CUDA-event time (ms) of fn() on `stream`, each launch bracketed."""
+    for _ in range(warm):
+        fn()
+    ms = []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.mean(ms)
+
+
+def measure_ceilings(torch, dev, stream, full, grads0, h_grads):
+    """Stream ceilings measured in the same run, for reading the kernels'
+    fractions: a write-only stream over R full-unit bf16 buffers with the
+    all-gather's store pattern (the library's fsdp_write_stream helper; the
+    write side that bounds the gather and the all-reduce), torch's own fill
+    kernels on the same buffers for comparison, a device copy of R buffers,
+    and the pinned host <-> device link (copy engines) on every unit's R
+    host gradient buffers."""
+    from fully_sharded_state_gb300 import capi
+    R = len(full)
+    P = full[0].numel()
+    with torch.cuda.stream(stream):
+        wr = timed_launches(torch, stream, lambda: capi.fsdp_write_stream(full, stream=stream),
+                            n=10)
+        zero = timed_launches(torch, stream, lambda: [f.zero_() for f in full], n=10)
+        fill = timed_launches(torch, stream, lambda: [f.fill_(1.5) for f in full], n=10)
+        cp = timed_launches(torch, stream,
+                            lambda: [f.copy_(g[:P]) for f, g in zip(full, grads0)], n=10)
+        h2d = [timed_launches(torch, stream,
+                              lambda hu=hu: [f[:h.numel()].copy_(h, non_blocking=True)
+                                             for f, h in zip(full, hu)], n=3, warm=1)
+               for hu in h_grads]
+        d2h = timed_launches(torch, stream, lambda: [h.copy_(f[:h.numel()], non_blocking=True)
+                                                     for f, h in zip(full, h_grads[0])], n=3)
+    nh = [sum(h.numel() * 2 for h in hu) for hu in h_grads]
+    gbs = lambda b, ms: round(b / (ms * 1e-3) / 1e9, 1)
+    return {"write_only_x_R_gbs": gbs(R * P * 2, wr),
+            "torch_zero_x_R_gbs": gbs(R * P * 2, zero), "torch_fill_x_R_gbs": gbs(R * P * 2, fill),
+            "device_copy_x_R_gbs": gbs(R * P * 4, cp),
+            "h2d_pinned_gbs": gbs(nh[0], h2d[0]),
+            "h2d_pinned_gbs_per_unit": [gbs(b, ms) for b, ms in zip(nh, h2d)],
+            "d2h_pinned_gbs": gbs(nh[0], d2h),
+            "how": f"fsdp_write_stream (32-byte stores, the gather's grid) and torch zero_ / "
+                   f"fill_ over {R} x {P:,} bf16; torch copy_ of {R} x {P:,} bf16 "
+                   f"(read + write bytes); pinned host <-> device copies of each unit's {R} x "
+                   f"{P:,} bf16 gradients; CUDA events, mean of 10 (3 for host copies)"}
+
+
+def peak_memory(torch, dev, unit_shapes, R, mode, hp, seed=11):
+    """Peak device memory of one training step of the engine against the
+    FSDP2 page's formula (§01): M_peak ~= M_shard + M_largest_unsharded +
+    M_prefetch + M_a + M_temp. Per unit and for all R virtual ranks (they
+    share this GPU): M_shard = R*S*14 B (bf16 shard, fp32 master, m, v; the
+    reduce-scatter's fp32 output lives in registers, so no sharded gradient
+    is stored); the largest unsharded unit = R full bf16 buffers; the
+    prefetch buffer = one more set (prefetch schedule only); M_temp = one
+    unit's R full bf16 gradients, which exist from the unit's backward to its
+    reduce-scatter; no activations. Two schedules of one step: forward
+    gathers every unit, backward walks the units in reverse, re-gathers each
+    one, produces its gradients and reduce-scatters them; "prefetch" issues
+    the next unit's gather together with the current unit's reduce-scatter
+    (fsdp_reduce_scatter_adamw_gather) into a second set of full buffers.
+    measured = peak of the bytes requested from torch's allocator during the
+    step; allocator_bytes = its max_memory_allocated (with block rounding)."""
+    from fully_sharded_state_gb300 import ShardedUnit
+
+    def requested(key):
+        # bytes the program asked for (the allocator's own rounding and
+        # segment slack are left out; max_memory_allocated counts them)
+        return torch.cuda.memory_stats(dev).get(f"requested_bytes.all.{key}", 0)
+
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = requested("current")
+    base_alloc = torch.cuda.memory_allocated(dev)
+    units = []
+    for u, shapes in enumerate(unit_shapes):
+        U = ShardedUnit(shapes, R, mode, "bf16", "bf16", device=dev)
+        w = torch.empty(U.P, dtype=torch.float32, device=dev).normal_(0.0, 0.02)
+        U.shard_from_full(w)
+        del w
+        units.append(U)
+    torch.cuda.synchronize(dev)
+    P_max = max(U.P for U in units)
+    m_shard = sum(R * U.S * (2 + 4 + 4 + 4) for U in units)
+    out = {}
+    for schedule in ("in_order", "prefetch"):
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        nsets = 2 if schedule == "prefetch" else 1
+        sets = [[torch.empty(P_max, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+                for _ in range(nsets)]
+        view = lambda k, U: [f[:U.P] for f in sets[k % nsets]]
+        for k, U in enumerate(units):  # forward
+            U.all_gather(view(k, U))
+        n = len(units)
+        if schedule == "in_order":
+            for k in reversed(range(n)):  # backward
+                U = units[k]
+                U.all_gather(view(k, U))
+                g = [torch.empty(U.P, dtype=torch.bfloat16, device=dev).normal_(0.0, 1e-3)
+                     for _ in range(R)]
+                U.reduce_scatter_adamw(g, hp)
+                del g
+        else:
+            units[n - 1].all_gather(view(n - 1, units[n - 1]))
+            for k in reversed(range(n)):
+                U = units[k]
+                g = [torch.empty(U.P, dtype=torch.bfloat16, device=dev).normal_(0.0, 1e-3)
+                     for _ in range(R)]
+                if k > 0:
+                    U.reduce_scatter_adamw_and_gather(g, hp, units[k - 1],
+                                                      view(k - 1, units[k - 1]))
+                else:
+                    U.reduce_scatter_adamw(g, hp)
+                del g
+        torch.cuda.synchronize(dev)
+        measured = requested("peak") - base
+        allocated = torch.cuda.max_memory_allocated(dev) - base_alloc
+        largest = R * P_max * 2
+        formula = m_shard + largest + (largest if nsets == 2 else 0) + R * P_max * 2
+        out[schedule] = {"measured_bytes": int(measured), "formula_bytes": int(formula),
+                         "allocator_bytes": int(allocated),
+                         "M_shard": int(m_shard), "M_largest_unsharded": int(largest),
+                         "M_prefetch": int(largest if nsets == 2 else 0),
+                         "M_temp_gradients": int(R * P_max * 2), "M_activations": 0,
+                         "measured_over_formula": round(measured / formula, 6)}
+        del sets
+    del units
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+def config_entry(torch, dev, stream, name, hp, peak, peak_src):
+    """One workload of the benchmark's configurations, timed as a training
+    step (every unit's all-gather + unflatten, then its reduce-scatter +
+    AdamW) with plain per-unit calls and, for several units, with the
+    prepared multi-unit calls (two launches per step); 50 steps back to back
+    between two CUDA events."""
+    from fully_sharded_state_gb300 import (ShardedUnit, prepare_all_gather_units,
+                                           prepare_reduce_scatter_adamw_units, synth)
+    wl = synth.WORKLOADS[name]
+    R = wl.R
+    bf16p, bf16g = wl.param_dtype == "bf16", wl.grad_dtype == "bf16"
+    pb, gb = (2 if bf16p else 4), (2 if bf16g else 4)
+    units, grads = [], []
+    for u in range(len(wl.units)):
+        U = ShardedUnit(wl.unit_shapes(u), R, wl.mode, wl.param_dtype, wl.grad_dtype, device=dev)
+        U.shard_from_full(synth.device_weights(wl, u, dev))
+        units.append(U)
+        grads.append(synth.device_grads(wl, u, dev))
+    fulls = [U.alloc_full() for U in units]
+    ag = sum(all_gather_bytes(U.P, R, pb) for U in units)
+    rs = sum(rs_adamw_bytes(U.P, R, gb, 2 if bf16p else 0) for U in units)
+    distinct = sum(R * U.P * (gb + pb) + R * U.S * (12 + (2 if bf16p else 0)) for U in units)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def step():
+        for k, U in enumerate(units):
+            U.all_gather(fulls[k], stream=stream)
+            U.reduce_scatter_adamw(grads[k], hp, stream=stream)
+
+    ms = timed_back_to_back(torch, stream, step)
+    gbs = (ag + rs) / (ms * 1e-3) / 1e9
+    e = {"workload": name, "cfg": wl.cfg, "units": len(units), "params_per_unit": units[0].P,
+         "R": R, "mode": wl.mode, "dtypes": f"{wl.param_dtype} params / {wl.grad_dtype} grads",
+         "algorithmic_bytes_per_step": int(ag + rs), "distinct_bytes": int(distinct),
+         "l2_resident": bool(distinct < l2), "ms_per_step": round(ms, 4),
+         "achieved": round(gbs, 1), "unit": UNIT, "frac": round(gbs / peak, 4),
+         "peak_source": peak_src, "gpu_launches_per_step": 2 * len(units),
+         "calls": "plain per-unit calls"}
+    if len(units) > 1:
+        ag_call = prepare_all_gather_units(units, fulls)
+        rs_call = prepare_reduce_scatter_adamw_units(units, grads)
+
+        def step_units():
+            ag_call(stream=stream)
+            rs_call(hp, stream=stream)
+
+        ms_u = timed_back_to_back(torch, stream, step_units)
+        gbs_u = (ag + rs) / (ms_u * 1e-3) / 1e9
+        e["all_units_per_call"] = {"ms_per_step": round(ms_u, 4), "achieved": round(gbs_u, 1),
+                                   "frac": round(gbs_u / peak, 4), "gpu_launches_per_step": 2,
+                                   "calls": "prepared multi-unit calls"}
+    if not e["l2_resident"] and ms > 0 and gbs < 0.5 * peak:
+        e["note"] = "launch-latency bound (small units)"
+    if name == "toy":
+        e["note"] = "eight elements per step: launch-latency bound, reported for completeness"
+    del units, grads, fulls
+    return e
+
+
 def run_ours(args):
     import torch
     from fully_sharded_state_gb300 import AdamWHP, ShardedUnit, build, capi, synth
@@ -296,8 +569,16 @@ def run_ours(args):
     desc, units_spec, wl = workload_units(args.workload)
     R = wl.R
     hp = AdamWHP(wl.lr, wl.betas[0], wl.betas[1], wl.eps, wl.weight_decay)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_src = measured_peak()
+
+    memory = None
+    if not args.no_memory:
+        memory = peak_memory(torch, dev, [[s for _, s in spec] for spec in units_spec], R,
+                             "per_param", hp)
 
     units, grads, pack_ms = [], [], []
+    w_unit0 = None
     for u, spec in enumerate(units_spec):
         U = ShardedUnit([s for _, s in spec], R, "per_param", "bf16", "bf16", device=dev,
                         names=[n for n, _ in spec])
@@ -308,13 +589,14 @@ def run_ours(args):
         b.record()
         b.synchronize()
         pack_ms.append(a.elapsed_time(b))
+        if u == 0 and rank == 0 and world == 1 and not args.no_cpu_baseline:
+            w_unit0 = w_full.cpu()
         del w_full
         units.append(U)
         grads.append([synth.device_normal(synth.seed("g", wl, u, r), U.P, wl.g_std, dev,
                                           torch.bfloat16) for r in range(R)])
     P_max = max(U.P for U in units)
     full = [torch.empty(P_max, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    stream = torch.cuda.current_stream(dev)
 
     ag_bytes = sum(all_gather_bytes(U.P, R) for U in units)
     rs_bytes = sum(rs_adamw_bytes(U.P, R) for U in units)
@@ -360,31 +642,25 @@ def run_ours(args):
              for k in range(len(units))]
     launches = args.steps * len(units) * 2
 
-    peak, peak_src = measured_peak()
     ms_step = elapsed_ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
 
-    def entry(kernel, nbytes, ms, traffic_key):
-        """Roofline record of one kernel: algorithmic bytes per launch over its
-        mean CUDA-event launch time, against the measured HBM peak."""
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": int(nbytes), "avg_launch_ms": round(ms, 4),
-                "traffic": profiled_traffic(traffic_key, args.workload) if traffic_key else None}
+    # host gradients of every unit, pinned (the end-to-end leg's inputs)
+    h_grads = None
+    if not args.no_e2e or not args.no_ceilings:
+        h_grads = [[torch.empty(U.P, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+                   for U in units]
+        for k, U in enumerate(units):
+            for r in range(R):
+                h_grads[k][r].copy_(grads[k][r])
+    ceilings = None
+    if not args.no_ceilings:
+        ceilings = measure_ceilings(torch, dev, stream, full, grads[0], h_grads)
 
-    def timed_launches(fn, n=20):
-        for _ in range(3):
-            fn()
-        ms = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            b.synchronize()
-            ms.append(a.elapsed_time(b))
-        return statistics.mean(ms)
+    def entry(kernel, nbytes, ms, traffic_key):
+        return roofline_entry(kernel, nbytes, ms, peak, peak_src,
+                              profiled_traffic(traffic_key, args.workload) if traffic_key
+                              else None, ceilings)
 
     roofline = entry("rs_adamw_kernel (fused reduce-scatter + AdamW)", rs_bytes / len(units),
                      statistics.mean(rs_ms), "rs_adamw")
@@ -395,7 +671,8 @@ def run_ours(args):
     # bf16 gradients into R fp32 full outputs (reduce dtype fp32)
     U0 = units[0]
     ar_out = [torch.empty(U0.P, dtype=torch.float32, device=dev) for _ in range(R)]
-    ar_ms = timed_launches(lambda: U0.all_reduce(grads[0], ar_out, "f32", stream=stream))
+    ar_ms = timed_launches(torch, stream,
+                           lambda: U0.all_reduce(grads[0], ar_out, "f32", stream=stream))
     del ar_out
     ddp = entry("all_reduce_kernel (DDP all-reduce: bf16 grads -> fp32 outputs)",
                 R * U0.P * (2 + 4), ar_ms, "all_reduce")
@@ -404,9 +681,11 @@ def run_ours(args):
     # the fp32 accumulators, and the last micro-batch fused into the step
     acc = U0.alloc_accumulators()
     U0.accumulate_grad(grads[0], acc, first=True, stream=stream)
-    acc_ms = timed_launches(lambda: U0.accumulate_grad(grads[0], acc, first=False, stream=stream))
-    rsacc_ms = timed_launches(lambda: U0.reduce_scatter_adamw_accum(acc, grads[0], hp,
-                                                                     stream=stream))
+    acc_ms = timed_launches(torch, stream,
+                            lambda: U0.accumulate_grad(grads[0], acc, first=False, stream=stream))
+    rsacc_ms = timed_launches(torch, stream,
+                              lambda: U0.reduce_scatter_adamw_accum(acc, grads[0], hp,
+                                                                    stream=stream))
     del acc
     accumulation = {
         "accumulate": entry("accumulate_kernel (acc += bf16 micro-batch grads, R ranks)",
@@ -418,15 +697,27 @@ def run_ours(args):
                  "step)", U0.P * 4 + R * U0.S * (4 + 2), statistics.mean(pack_ms[1:] or pack_ms),
                  "pack")
 
-    small = None if args.no_small else small_configs(dev, hp)
-
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes)
+        e2e = run_e2e(args, units, grads, h_grads, full, hp, stream, dev, world, step_bytes)
+
+    configs = None
+    if not args.no_configs:
+        configs = {"llama4": {
+            "workload": "llama4", "cfg": 5, "units": len(units), "params_per_unit": U0.P,
+            "R": R, "mode": "per_param", "dtypes": "bf16 params / bf16 grads",
+            "algorithmic_bytes_per_step": int(step_bytes), "l2_resident": False,
+            "ms_per_step": round(ms_step, 4), "achieved": round(value / world, 1), "unit": UNIT,
+            "frac": round(value / world / peak, 4), "peak_source": peak_src,
+            "gpu_launches_per_step": 2 * len(units), "calls": "plain per-unit calls",
+            "note": "the headline workload: see value and roofline"}} \
+            if args.workload == "llama4" else {}
+        for name in ("toy", "block", "block12_flat", "ragged"):
+            configs[name] = config_entry(torch, dev, stream, name, hp, peak, peak_src)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl)
+    if w_unit0 is not None:
+        cpu = cpu_baseline(wl, [s for _, s in units_spec[0]], w_unit0, grads[0])
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -440,9 +731,10 @@ def run_ours(args):
                            "l2": "inputs larger than L2 (>= 3.9 GB streamed per launch); no flush",
                            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
                 "pct_of_hbm_peak": round(value / world / peak, 4),
+                "pct_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
-                "grad_accumulation": accumulation, "pack": pack,
-                "l2_resident_configs": small,
+                "grad_accumulation": accumulation, "pack": pack, "ceilings": ceilings,
+                "configs": configs, "peak_memory": memory,
                 "clocks": clocks.summary(), "gpu_launches": launches,
                 "cpu_baseline": cpu, "e2e": e2e}
         print(json.dumps(line), flush=True)
@@ -451,69 +743,24 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def small_configs(dev, hp):
-    """The smaller workloads, whose units fit in the 129 MB L2: one 512/8/2048
-    TransformerBlock (FSDP2, R=4) and twelve of them as FSDP1 FlatParameters
-    (R=4). Flagged as L2-resident; they are parity workloads, reported for
-    context, not the headline."""
-    import torch
-    from fully_sharded_state_gb300 import ShardedUnit, synth
-    out = {}
-    for name in ("block", "block12_flat"):
-        wl = synth.WORKLOADS[name]
-        units = [ShardedUnit(wl.unit_shapes(u), wl.R, wl.mode, "bf16", "bf16", device=dev)
-                 for u in range(len(wl.units))]
-        grads = []
-        for u, U in enumerate(units):
-            U.shard_from_full(synth.device_normal(synth.seed("w", wl, u), U.P, wl.w_std, dev))
-            grads.append([synth.device_normal(synth.seed("g", wl, u, r), U.P, wl.g_std, dev,
-                                              torch.bfloat16) for r in range(wl.R)])
-        full = [torch.empty(units[0].P, dtype=torch.bfloat16, device=dev) for _ in range(wl.R)]
-
-        def step():
-            for k, U in enumerate(units):
-                U.all_gather(full)
-                U.reduce_scatter_adamw(grads[k], hp)
-
-        for _ in range(5):
-            step()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record()
-        for _ in range(50):
-            step()
-        b.record()
-        b.synchronize()
-        ms = a.elapsed_time(b) / 50
-        nbytes = sum(all_gather_bytes(U.P, wl.R) + rs_adamw_bytes(U.P, wl.R) for U in units)
-        out[name] = {"units": len(units), "params_per_unit": units[0].P, "R": wl.R,
-                     "mode": wl.mode, "ms_per_step": round(ms, 4),
-                     "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
-                     "l2_resident": True, "gpu_launches_per_step": 2 * len(units)}
-        del units, grads, full
-    return out
-
-
-def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
+def run_e2e(args, units, grads, h_grads, full, hp, stream, dev, world, step_bytes):
     """The same step through the public API from host buffers. Every step
-    copies each unit's R gradients from pinned host memory to the device on a
-    copy stream (each unit's copy waits only for the previous step's
+    copies each unit's own R gradients from pinned host memory to the device
+    on two copy streams (each unit's copy waits only for the previous step's
     reduce-scatter of that unit, so copies run ahead of the kernels), runs
     the unit's all-gather and reduce-scatter + AdamW once its copy is done,
     and reads its updated bf16 parameter shards back into pinned host memory
-    on a third stream."""
+    on a third stream. As many steps as the device-timed region."""
     import torch
     R = units[0].R
-    P_max = max(U.P for U in units)
-    h_grads = [torch.empty(P_max, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
-    for r in range(R):
-        h_grads[r].copy_(grads[0][r][:P_max].cpu())
     h_out = [[torch.empty(U.S, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
              for U in units]
     h2d = sum(R * U.P * 2 for U in units)
     d2h = sum(R * U.S * 2 for U in units)
-    steps = max(2, min(args.steps, args.e2e_steps))
-    h2d_stream = torch.cuda.Stream(dev)
+    steps = args.steps
+    # two copy streams: one stream's host-to-device copies reach ~178 GB/s on
+    # GB300, two together the link's ~211 GB/s
+    h2d_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
     d2h_stream = torch.cuda.Stream(dev)
     rs_done = [torch.cuda.Event() for _ in units]
     d2h_done = [torch.cuda.Event() for _ in units]
@@ -523,15 +770,19 @@ def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
     def e2e_step():
         copied = []
         for k, U in enumerate(units):
-            h2d_stream.wait_event(rs_done[k])  # the buffer's last reader
-            with torch.cuda.stream(h2d_stream):
-                for r in range(R):
-                    grads[k][r].copy_(h_grads[r][:U.P], non_blocking=True)
-            e = torch.cuda.Event()
-            e.record(h2d_stream)
-            copied.append(e)
+            evs = []
+            for c, hs in enumerate(h2d_streams):
+                hs.wait_event(rs_done[k])  # the buffer's last reader
+                with torch.cuda.stream(hs):
+                    for r in range(c, R, len(h2d_streams)):
+                        grads[k][r].copy_(h_grads[k][r], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(hs)
+                evs.append(e)
+            copied.append(evs)
         for k, U in enumerate(units):
-            stream.wait_event(copied[k])
+            for e in copied[k]:
+                stream.wait_event(e)
             stream.wait_event(d2h_done[k])  # last step's read-back of this unit's shards
             U.all_gather([f[:U.P] for f in full], stream=stream)
             U.reduce_scatter_adamw(grads[k], hp, stream=stream)
@@ -555,9 +806,9 @@ def run_e2e(args, units, grads, full, hp, stream, dev, world, step_bytes):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1e3 * dt / steps, 3),
             "h2d_GBps": round(h2d * steps / dt / 1e9, 1),
-            "path": "pinned host grads -> device on a copy stream running ahead, per-unit "
-                    "all-gather + reduce-scatter/AdamW on the compute stream, bf16 shards -> "
-                    "pinned host on a third stream; host wall clock"}
+            "path": "each unit's own pinned host grads -> device on two copy streams running "
+                    "ahead, per-unit all-gather + reduce-scatter/AdamW on the compute stream, "
+                    "bf16 shards -> pinned host on a fourth stream; host wall clock"}
 
 
 def main(argv=None):
@@ -567,10 +818,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama4", choices=["llama4", "llama_attn"])
-    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-small", action="store_true", help="skip the L2-resident configs")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-memory", action="store_true", help="skip the peak-memory step")
+    ap.add_argument("--no-ceilings", action="store_true", help="skip the stream ceilings")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -105,6 +105,9 @@ def load(path: str = LIB_PATH):
         ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
         ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
         ctypes.POINTER(AdamWHP), ctypes.c_int64, _vp]
+    L.fsdp_write_stream.restype = ctypes.c_int
+    L.fsdp_write_stream.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int64,
+                                    ctypes.c_uint32, _vp]
     L.fsdp_last_error.restype = ctypes.c_char_p
     L.fsdp_last_error.argtypes = []
     L.fsdp_version.restype = ctypes.c_char_p
@@ -490,6 +493,20 @@ def prepare_fsdp_reduce_scatter_adamw_units(layouts, grad_full, master, m, v, pa
                         (g, ma, mm, vv, ps, gs),
                         (list(layouts), grad_full, master, m, v, param_shard_out,
                          grad_shard_out), True)
+
+
+def fsdp_write_stream(dst, pattern: int = 0x3FC03FC0, stream=None) -> None:
+    """Measurement helper: write a 32-bit pattern over every tensor in
+    ``dst`` (equal sizes, a multiple of 32 bytes) with the all-gather's store
+    pattern, to time the write-only stream ceiling."""
+    if not dst:
+        raise FsdpArgumentError("dst: need at least one tensor")
+    nbytes = dst[0].numel() * dst[0].element_size()
+    a = _Args()
+    arr = a.array(dst, len(dst), "dst", dst[0].numel(), FSDP_BF16 if dst[0].element_size() == 2
+                  else FSDP_F32)
+    _check(load().fsdp_write_stream(arr, len(dst), nbytes, pattern & 0xFFFFFFFF,
+                                    _stream_handle(stream)))
 
 
 def fsdp_version() -> str:

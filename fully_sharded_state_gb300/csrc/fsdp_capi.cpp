@@ -11,6 +11,8 @@
 #include <new>
 #include <string>
 
+#include <cuda_runtime.h>
+
 #include "fsdp_internal.h"
 
 namespace fsdp {
@@ -188,6 +190,37 @@ fsdp_status check_overlap(std::vector<Span> &spans)
             far_out = &s;
     }
     return FSDP_OK;
+}
+
+// Every buffer must be device memory of one device (the one the call runs
+// on). A host or peer pointer would otherwise reach a kernel.
+fsdp_status check_devices(const std::vector<Span> &spans)
+{
+    int dev = -1;
+    for (const Span &s : spans) {
+        cudaPointerAttributes a;
+        cudaError_t err = cudaPointerGetAttributes(&a, reinterpret_cast<const void *>(s.lo));
+        if (err != cudaSuccess)
+            return set_error(FSDP_ECUDA, "cudaPointerGetAttributes(%s[%d]): %s", s.what, s.rank,
+                             cudaGetErrorString(err));
+        if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+            return set_error(FSDP_EINVAL, "%s[%d] = %p is not device memory", s.what, s.rank,
+                             reinterpret_cast<const void *>(s.lo));
+        if (dev < 0)
+            dev = a.device;
+        else if (a.device != dev)
+            return set_error(FSDP_EINVAL, "%s[%d] is on device %d, other buffers on device %d",
+                             s.what, s.rank, a.device, dev);
+    }
+    return FSDP_OK;
+}
+
+// The checks every call makes once its spans are collected: no output
+// overlaps another buffer, and all buffers are on one device.
+fsdp_status check_spans(std::vector<Span> &spans)
+{
+    fsdp_status st = check_overlap(spans);
+    return st != FSDP_OK ? st : check_devices(spans);
 }
 
 fsdp_status check_gather_args(const fsdp_layout_t *L, const void *const *shard,
@@ -477,7 +510,7 @@ fsdp_status fsdp_pack_flat(const fsdp_layout_t *L, const float *full, void *cons
         return set_error(FSDP_EINVAL, "fsdp_pack_flat: param_shard must be NULL for an F32 "
                                       "layout (the master is the parameter shard)");
     }
-    if ((st = check_overlap(spans)) != FSDP_OK)
+    if ((st = check_spans(spans)) != FSDP_OK)
         return st;
     return launch_pack(L, full, param_shard, master, stream);
 }
@@ -492,7 +525,7 @@ fsdp_status fsdp_all_gather_unflatten(const fsdp_layout_t *L, const void *const 
     std::vector<Span> spans;
     fsdp_status st = check_gather_args(L, shard, full_out, &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     return launch_all_gather(1, &L, shard, full_out, stream);
@@ -511,7 +544,7 @@ fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *L, const void *const 
     std::vector<Span> spans;
     st = check_rs_args(L, grad_full, master, m, v, param_shard_out, grad_shard_out, &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     return launch_rs_adamw(1, &L, grad_full, master, m, v, param_shard_out, grad_shard_out,
@@ -535,7 +568,7 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
     if (st == FSDP_OK && G->P > 0)
         st = check_gather_args(G, shard, full_out, &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     if (L->P == 0)
@@ -563,7 +596,7 @@ fsdp_status fsdp_all_reduce(const fsdp_layout_t *L, const void *const *grad_full
         st = check_ptrs((const void *const *)out, L->R, L->P * esize(out_dtype), true, "out",
                         &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     return launch_all_reduce(L, grad_full, out, out_dtype, stream);
@@ -582,7 +615,7 @@ fsdp_status fsdp_accumulate_grad(const fsdp_layout_t *L, float *const *acc_full,
     if (st == FSDP_OK)
         st = check_ptrs((const void *const *)acc_full, L->R, L->P * 4, true, "acc_full", &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     return launch_accumulate(L, acc_full, grad_full, first, stream);
@@ -605,7 +638,7 @@ fsdp_status fsdp_reduce_scatter_adamw_accum(const fsdp_layout_t *L, const float 
     if (st == FSDP_OK)
         st = check_rs_args(L, grad_full, master, m, v, param_shard_out, grad_shard_out, &spans);
     if (st == FSDP_OK)
-        st = check_overlap(spans);
+        st = check_spans(spans);
     if (st != FSDP_OK)
         return st;
     return launch_rs_adamw(1, &L, grad_full, master, m, v, param_shard_out, grad_shard_out,
@@ -641,7 +674,7 @@ fsdp_status fsdp_all_gather_unflatten_units(int n_units, const fsdp_layout_t *co
     }
     if (Ls.empty())
         return FSDP_OK;
-    if ((st = check_overlap(spans)) != FSDP_OK)
+    if ((st = check_spans(spans)) != FSDP_OK)
         return st;
     return launch_all_gather((int)Ls.size(), Ls.data(), sh.data(), fo.data(), stream);
 }
@@ -691,11 +724,32 @@ fsdp_status fsdp_reduce_scatter_adamw_units(int n_units, const fsdp_layout_t *co
     }
     if (Ls.empty())
         return FSDP_OK;
-    if ((st = check_overlap(spans)) != FSDP_OK)
+    if ((st = check_spans(spans)) != FSDP_OK)
         return st;
     return launch_rs_adamw((int)Ls.size(), Ls.data(), g.data(), ma.data(), mm.data(), vv.data(),
                            data_or_null(ps, param_shard_out), data_or_null(gs, grad_shard_out),
                            adam_scalars(hp, step, R), stream, nullptr);
+}
+
+fsdp_status fsdp_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,
+                              void *stream)
+{
+    if (dst == nullptr || n < 1 || n > FSDP_MAX_RANKS || bytes < 0)
+        return set_error(FSDP_EINVAL, "fsdp_write_stream: bad arguments");
+    if (bytes % 32 != 0)
+        return set_error(FSDP_EINVAL, "fsdp_write_stream: bytes must be a multiple of 32");
+    if (bytes == 0)
+        return FSDP_OK;
+    std::vector<Span> spans;
+    for (int d = 0; d < n; d++)
+        if (dst[d] != nullptr && (reinterpret_cast<uintptr_t>(dst[d]) & 31u))
+            return set_error(FSDP_EALIGN, "fsdp_write_stream: dst[%d] is not 32-byte aligned", d);
+    fsdp_status st = check_ptrs((const void *const *)dst, n, bytes, true, "dst", &spans);
+    if (st == FSDP_OK)
+        st = check_spans(spans);
+    if (st != FSDP_OK)
+        return st;
+    return launch_write_stream(dst, n, bytes, pattern, stream);
 }
 
 }  // extern "C"

@@ -35,18 +35,18 @@ constexpr int kMaxR = FSDP_MAX_RANKS;
 // Resident CTAs per SM of each kernel's persistent grid. Measured on GB300
 // with 218M-parameter Llama units, R = 8 (one launch per point):
 //   reduce-scatter + AdamW: 2/SM 1.520 ms, 3/SM 1.389 ms, 4/SM (the register
-//   limit) 1.498 ms;  all-gather: 2/SM 0.655 ms, 3/SM 0.690 ms, 8/SM (the
-//   limit) 0.690 ms.
+//   limit) 1.498 ms.
 // Fewer CTAs, each streaming its tiles in order, keep a narrower window of
 // every buffer open at once; past these points HBM does not go faster.
 constexpr int kRsCtasPerSm = 3;
+// all-gather: CTAs of kGatherThreads (128) threads.
 constexpr int kGatherCtasPerSm = 2;
 // pack (set-up): 1/SM 0.810, 2/SM 0.482, 3/SM 0.404, 4/SM 0.356, 6/SM
 // 0.421, 8/SM 0.418 ms.
 constexpr int kPackCtasPerSm = 4;
-// all-reduce (bf16 grads -> fp32 outputs): 1/SM 1.826, 2/SM 1.744, 3/SM
-// 1.941, 4/SM 1.904, 8/SM 1.976 ms.
-constexpr int kAllReduceCtasPerSm = 2;
+// all-reduce (bf16 grads -> fp32 outputs), pipelined with 32-byte stores:
+// 1/SM 1.575 ms, 2/SM 1.676 ms, 3/SM 1.665 ms (a replica of the kernel).
+constexpr int kAllReduceCtasPerSm = 1;
 constexpr int kAccumulateCtasPerSm = 3;
 
 struct PackParams {
@@ -63,6 +63,7 @@ struct GatherParams {
     const unsigned char *shard[kMaxR];
     unsigned char *full[kMaxR];
     int R;
+    int wide;  // every shard and full pointer is 32-byte aligned
     int nseg;
     int64_t total_tiles;
     Seg seg[kMaxSegsPerLaunch];
@@ -168,9 +169,9 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ PackParams p)
 {
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        Tile T = locate(p.seg, p.nseg, t, true);
-        float *dst = p.master[T.base + T.rank] + T.sbase;
-        uint16_t *dst16 = kBf16 ? p.pshard[T.base + T.rank] + T.sbase : nullptr;
+        const Tile T = locate(p.seg, p.nseg, t, true);  // one unit: base 0
+        float *dst = p.master[T.rank] + T.sbase;
+        uint16_t *dst16 = kBf16 ? p.pshard[T.rank] + T.sbase : nullptr;
         const float *src = p.full + T.fbase;
         const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
         const bool aligned = ((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0;
@@ -223,70 +224,139 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
 }
 
 // ----------------------------------------------------- all-gather ----------
+//
+// The gather writes R bytes for every byte it reads, so its store pattern
+// sets its speed. It runs 128-thread CTAs, each thread owning 16 consecutive
+// elements of a tile: with 32-byte aligned buffers every store instruction
+// writes whole 32-byte sectors (one 32-byte vector per destination for
+// bf16, two for fp32). Two 16-byte halves of one sector written by separate
+// instructions cost about 1.8x the DRAM time of whole-sector writes on GB300
+// (a write-only stream of 8 fp32 buffers: 3.7 TB/s with 16-byte halves,
+// 6.5 TB/s with 32-byte stores). Tiles that are only 16-byte aligned use
+// 16-byte vectors laid out so that a warp's instruction still covers 512
+// contiguous bytes; other tiles copy element by element.
+
+constexpr int kGatherThreads = 128;
+constexpr int kGatherEPT = 16;
+static_assert(kGatherThreads * kGatherEPT == kTile, "a gather CTA covers one tile");
 
 template <int kEB> struct ElemOf;
 template <> struct ElemOf<2> { using T = unsigned short; };
 template <> struct ElemOf<4> { using T = unsigned int; };
 
+__device__ __forceinline__ void ld32(const void *p, uint4 &a, uint4 &b)
+{
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                   "=r"(b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
+{
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x),
+                 "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
 // One all-gather tile: the tile's shard elements go to the same place of
 // every destination's full buffer. kEB = element bytes (2 bf16, 4 fp32); the
-// copy is bitwise. PP is any parameter block with `shard` and `full`.
+// copy is bitwise. PP is any parameter block with `shard`, `full` and `wide`
+// (1 when every shard and full pointer of the launch is 32-byte aligned).
 template <int RC, int kEB, class PP>
 __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
 {
     using E = typename ElemOf<kEB>::T;
-    constexpr int kVecs = kElemsPerThread * kEB / 16;  // 16-byte vectors per thread
+    constexpr int kV = 16 / kEB;                     // elements per 16-byte vector
+    constexpr int kW = 32 / kEB;                     // elements per 32-byte vector
+    constexpr int kWide = kGatherEPT / kW;           // 32-byte vectors per thread
+    constexpr int kNarrow = kTile / (kGatherThreads * kV);  // 16-byte vectors per thread
+    const int n = RC > 0 ? RC : R;
     const E *src = reinterpret_cast<const E *>(p.shard[T.base + T.rank]) + T.sbase;
+    // destination pointers in registers when R is known at compile time
+    constexpr int kN = RC > 0 ? RC : 1;
+    unsigned char *fl[kN];
     unsigned char *const *full = p.full + T.base;
-    if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0) {
-        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
-        if (e + kElemsPerThread <= T.len) {
-            uint4 x[kVecs];
+    if (RC > 0) {
 #pragma unroll
-            for (int k = 0; k < kVecs; k++)
-                x[k] = ld_stream(src + e + k * (16 / kEB));
-            if (RC > 0) {
+        for (int d = 0; d < kN; d++)
+            fl[d] = p.full[T.base + d];
+        full = fl;
+    }
+    const int64_t off = T.fbase | T.sbase;
+    const int tid = threadIdx.x;
+    if (p.wide && (off & (kW - 1)) == 0) {
+        const int64_t e = (int64_t)tid * kGatherEPT;
+        if (e + kGatherEPT <= T.len) {
+            uint4 x[kWide][2];
 #pragma unroll
-                for (int d = 0; d < (RC > 0 ? RC : 1); d++) {
-                    E *dst = reinterpret_cast<E *>(full[d]) + T.fbase + e;
+            for (int k = 0; k < kWide; k++)
+                ld32(src + e + k * kW, x[k][0], x[k][1]);
+#pragma unroll 8
+            for (int d = 0; d < n; d++) {
+                E *dst = reinterpret_cast<E *>(full[d]) + T.fbase + e;
 #pragma unroll
-                    for (int k = 0; k < kVecs; k++)
-                        st_stream(dst + k * (16 / kEB), x[k]);
-                }
-            } else {
-                for (int d = 0; d < R; d++) {
-                    E *dst = reinterpret_cast<E *>(full[d]) + T.fbase + e;
-#pragma unroll
-                    for (int k = 0; k < kVecs; k++)
-                        st_stream(dst + k * (16 / kEB), x[k]);
-                }
+                for (int k = 0; k < kWide; k++)
+                    st32(dst + k * kW, x[k][0], x[k][1]);
             }
             return;
         }
-        for (int64_t q = e; q < T.len; q++) {
-            E x = src[q];
-            for (int d = 0; d < R; d++)
+        for (int64_t q = e; q < T.len && q < e + kGatherEPT; q++) {
+            const E x = src[q];
+            for (int d = 0; d < n; d++)
                 reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
         }
         return;
     }
+    if ((off & (kV - 1)) == 0) {
+        uint4 x[kNarrow];  // every load of this thread before its stores
 #pragma unroll
-    for (int k = 0; k < kElemsPerThread; k++) {
-        int64_t q = threadIdx.x + (int64_t)k * kThreads;
+        for (int k = 0; k < kNarrow; k++) {
+            const int64_t e = (int64_t)(tid + k * kGatherThreads) * kV;
+            if (e + kV <= T.len)
+                x[k] = ld_stream(src + e);
+        }
+#pragma unroll
+        for (int k = 0; k < kNarrow; k++) {
+            const int64_t e = (int64_t)(tid + k * kGatherThreads) * kV;
+            if (e + kV <= T.len) {
+#pragma unroll 8
+                for (int d = 0; d < n; d++)
+                    st_stream(reinterpret_cast<E *>(full[d]) + T.fbase + e, x[k]);
+            } else {
+                for (int64_t q = e; q < T.len; q++) {
+                    const E x = src[q];
+                    for (int d = 0; d < n; d++)
+                        reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
+                }
+            }
+        }
+        return;
+    }
+#pragma unroll 4
+    for (int k = 0; k < kGatherEPT; k++) {
+        const int64_t q = tid + (int64_t)k * kGatherThreads;
         if (q < T.len) {
-            E x = src[q];
-            for (int d = 0; d < R; d++)
+            const E x = src[q];
+            for (int d = 0; d < n; d++)
                 reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
         }
     }
 }
 
-template <int RC, int kEB>
-__global__ void __launch_bounds__(kThreads) all_gather_kernel(const __grid_constant__ GatherParams p)
+// kUnits: the launch holds several units (segments carry their unit's
+// pointer base); otherwise the base is a compile-time 0 and the per-rank
+// pointers are read from the parameter block at fixed offsets.
+template <int RC, int kEB, bool kUnits>
+__global__ void __launch_bounds__(kGatherThreads)
+    all_gather_kernel(const __grid_constant__ GatherParams p)
 {
     const int R = RC > 0 ? RC : p.R;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
-        gather_tile<RC, kEB>(p, R, locate(p.seg, p.nseg, t, false));
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        Tile T = locate(p.seg, p.nseg, t, false);
+        if (!kUnits)
+            T.base = 0;
+        gather_tile<RC, kEB>(p, R, T);
+    }
 }
 
 // ------------------------------------------- reduce-scatter + AdamW --------
@@ -459,7 +529,20 @@ __device__ __forceinline__ void fold8_accum(const RankPtrs &b, int R, int64_t j,
 template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
 {
-    const RankPtrs b = rank_ptrs(p, T);
+    RankPtrs b = rank_ptrs(p, T);
+    // With R known at compile time the unit's R gradient pointers are read
+    // from the parameter block into registers once per tile; the loads below
+    // then index registers, not the parameter block through a generic
+    // pointer (which cost ~4 % of a Llama unit's time). The accumulating
+    // form keeps the generic pointers: its rank loop is not fully unrolled.
+    constexpr int kN = RC > 0 ? RC : 1;
+    const void *gl[kN];
+    if (RC > 0 && !kAccum) {
+#pragma unroll
+        for (int q = 0; q < kN; q++)
+            gl[q] = p.grad[T.base + q];
+        b.grad = gl;
+    }
     if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
 #pragma unroll 1
         for (int k = 0; k < kElemsPerThread; k++) {
@@ -518,12 +601,17 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
     }
 }
 
-template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum>
+// kUnits as for the all-gather.
+template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
 __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constant__ RsParams p)
 {
     const int R = RC > 0 ? RC : p.R;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
-        rs_adamw_tile<RC, kGradBf16, kParamBf16, kAccum>(p, R, locate(p.seg, p.nseg, t, false));
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        Tile T = locate(p.seg, p.nseg, t, false);
+        if (!kUnits)
+            T.base = 0;
+        rs_adamw_tile<RC, kGradBf16, kParamBf16, kAccum>(p, R, T);
+    }
 }
 
 // ------------------------------------------------- gradient accumulation ----
@@ -579,62 +667,187 @@ __global__ void __launch_bounds__(kThreads) accumulate_kernel(const __grid_const
 // rank-ordered fp32 average of the R full gradients (or its bf16 rounding).
 // Tiles run over the flat unit index; every tile start is a multiple of
 // kTile, so only the unit's last partial vector takes the scalar path.
+//
+// With R known at compile time the kernel is software-pipelined: a thread
+// issues the R gradient loads of its next tile before the 2R (or R) stores
+// of the current one, so loads stay in flight while the stores drain; one
+// CTA per SM then keeps HBM busy. fp32 outputs are stored as one 32-byte
+// vector per rank when every output is 32-byte aligned (whole sectors; see
+// the all-gather). Measured on a Llama unit (R = 8, bf16 in, fp32 out):
+// 1.73 ms unpipelined with 16-byte stores at 2 CTAs/SM, 1.58 ms pipelined
+// with 32-byte stores at 1 CTA/SM.
 
 struct ReduceParams {
     const void *grad[kMaxR];
     void *out[kMaxR];
     float inv_R;
     int R;
+    int wide;  // every output pointer is 32-byte aligned
     int64_t P;
     int64_t total_tiles;
 };
 
+// R ranks' 8 gradient values at one index, held in registers: bf16 as one
+// 16-byte vector per rank, fp32 as two.
+template <int kR, bool kGradBf16> struct Grad8 {
+    uint4 v[kR][kGradBf16 ? 1 : 2];
+};
+
+template <int kR, bool kGradBf16, class PP>
+__device__ __forceinline__ void load_ranks8(const PP &p, int64_t j, Grad8<kR, kGradBf16> &g)
+{
+#pragma unroll
+    for (int q = 0; q < kR; q++) {
+        if (kGradBf16) {
+            g.v[q][0] = ld_stream(reinterpret_cast<const uint16_t *>(p.grad[q]) + j);
+        } else {
+            const float *f = reinterpret_cast<const float *>(p.grad[q]) + j;
+            g.v[q][0] = ld_stream(f);
+            g.v[q][kGradBf16 ? 0 : 1] = ld_stream(f + 4);
+        }
+    }
+}
+
+template <int kR, bool kGradBf16>
+__device__ __forceinline__ void fold_ranks8(const Grad8<kR, kGradBf16> &g, float acc[8])
+{
+#pragma unroll
+    for (int q = 0; q < kR; q++) {
+        float x[8];
+        if (kGradBf16) {
+            unpack_bf16x8(g.v[q][0], x);
+        } else {
+            const uint4 a = g.v[q][0], b = g.v[q][kGradBf16 ? 0 : 1];
+            x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+            x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+            x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+            x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            acc[k] = q == 0 ? x[k] : __fadd_rn(acc[k], x[k]);
+    }
+}
+
+// Stores one thread's 8 averaged values at unit index j to every output.
+template <bool kOutBf16>
+__device__ __forceinline__ void store_ranks8(const ReduceParams &p, int R, int64_t j,
+                                             const float acc[8])
+{
+    if (kOutBf16) {
+        uint4 b;
+        b.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
+        b.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
+        b.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
+        b.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
+#pragma unroll 8
+        for (int d = 0; d < R; d++)
+            st_stream(static_cast<uint16_t *>(p.out[d]) + j, b);
+        return;
+    }
+    const uint4 lo = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                __float_as_uint(acc[2]), __float_as_uint(acc[3]));
+    const uint4 hi = make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                __float_as_uint(acc[6]), __float_as_uint(acc[7]));
+    if (p.wide) {
+#pragma unroll 8
+        for (int d = 0; d < R; d++)
+            st32(static_cast<float *>(p.out[d]) + j, lo, hi);
+    } else {
+#pragma unroll 8
+        for (int d = 0; d < R; d++) {
+            st_stream(static_cast<float *>(p.out[d]) + j, lo);
+            st_stream(static_cast<float *>(p.out[d]) + j + 4, hi);
+        }
+    }
+}
+
+// Elements [base + e, base + len) one by one (the unit's last partial vector).
+template <bool kGradBf16, bool kOutBf16>
+__device__ __forceinline__ void all_reduce_scalar(const ReduceParams &p, int R, int64_t from,
+                                                  int64_t to)
+{
+    for (int64_t q = from; q < to; q++) {
+        float acc = load_grad<kGradBf16>(p.grad[0], q);
+        for (int r = 1; r < R; r++)
+            acc = __fadd_rn(acc, load_grad<kGradBf16>(p.grad[r], q));
+        acc = __fmul_rn(acc, p.inv_R);
+        for (int d = 0; d < R; d++) {
+            if (kOutBf16)
+                static_cast<uint16_t *>(p.out[d])[q] = f32_to_bf16_bits(acc);
+            else
+                static_cast<float *>(p.out[d])[q] = acc;
+        }
+    }
+}
+
 template <int RC, bool kGradBf16, bool kOutBf16>
 __global__ void __launch_bounds__(kThreads) all_reduce_kernel(const __grid_constant__ ReduceParams p)
 {
-    const int R = RC > 0 ? RC : p.R;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const int64_t base = t * kTile;
-        const int64_t len = p.P - base < kTile ? p.P - base : kTile;
-        const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
-        if (e + kElemsPerThread <= len) {
-            const int64_t j = base + e;
+    const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+    if constexpr (RC > 0) {
+        // a tile is "full" for this thread when its 8 elements exist
+        auto full = [&](int64_t t) { return t < p.total_tiles && t * kTile + e + 8 <= p.P; };
+        Grad8<RC, kGradBf16> g;
+        int64_t t = blockIdx.x;
+        if (full(t))
+            load_ranks8<RC, kGradBf16>(p, t * kTile + e, g);
+        for (; t < p.total_tiles; t += gridDim.x) {
+            const int64_t j = t * kTile + e;
+            if (!full(t)) {  // the unit's last, partial tile
+                all_reduce_scalar<kGradBf16, kOutBf16>(p, RC, j, p.P);
+                continue;
+            }
             float acc[8];
-            fold8<RC, kGradBf16>(p.grad, R, j, acc);
+            fold_ranks8<RC, kGradBf16>(g, acc);
+            const int64_t tn = t + gridDim.x;
+            if (full(tn))
+                load_ranks8<RC, kGradBf16>(p, tn * kTile + e, g);
 #pragma unroll
             for (int k = 0; k < 8; k++)
                 acc[k] = __fmul_rn(acc[k], p.inv_R);
-            if (kOutBf16) {
-                uint4 b;
-                b.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
-                b.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
-                b.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
-                b.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
-                for (int d = 0; d < R; d++)
-                    st_stream(static_cast<uint16_t *>(p.out[d]) + j, b);
-            } else {
-                const float4 lo = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                const float4 hi = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                for (int d = 0; d < R; d++) {
-                    st_f4(static_cast<float *>(p.out[d]) + j, lo);
-                    st_f4(static_cast<float *>(p.out[d]) + j + 4, hi);
-                }
+            store_ranks8<kOutBf16>(p, RC, j, acc);
+        }
+    } else {
+        const int R = p.R;
+        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+            const int64_t j = t * kTile + e;
+            if (j + 8 > p.P) {
+                all_reduce_scalar<kGradBf16, kOutBf16>(p, R, j, p.P);
+                continue;
             }
-        } else {
-            for (int64_t q = base + e; q < base + len; q++) {
-                float acc = load_grad<kGradBf16>(p.grad[0], q);
-                for (int r = 1; r < R; r++)
-                    acc = __fadd_rn(acc, load_grad<kGradBf16>(p.grad[r], q));
-                acc = __fmul_rn(acc, p.inv_R);
-                for (int d = 0; d < R; d++) {
-                    if (kOutBf16)
-                        static_cast<uint16_t *>(p.out[d])[q] = f32_to_bf16_bits(acc);
-                    else
-                        static_cast<float *>(p.out[d])[q] = acc;
-                }
-            }
+            float acc[8];
+            fold8<0, kGradBf16>(p.grad, R, j, acc);
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                acc[k] = __fmul_rn(acc[k], p.inv_R);
+            store_ranks8<kOutBf16>(p, R, j, acc);
         }
     }
+}
+
+// ------------------------------------------------------- write stream ----
+//
+// Measurement helper, not a step of the method: writes a 32-bit pattern to n
+// buffers with the all-gather's store pattern (one 32-byte vector per buffer
+// per thread, 128-thread CTAs, the gather's grid), so that the write-only
+// stream ceiling that bounds the gather and the all-reduce can be measured
+// in the same run as they are.
+
+struct WriteParams {
+    unsigned char *dst[kMaxR];
+    int n;
+    uint32_t pattern;
+    int64_t chunks;  // 32-byte chunks per buffer
+};
+
+__global__ void __launch_bounds__(kGatherThreads) write_stream_kernel(const __grid_constant__ WriteParams p)
+{
+    const uint4 v = make_uint4(p.pattern, p.pattern, p.pattern, p.pattern);
+    for (int64_t c = blockIdx.x * (int64_t)kGatherThreads + threadIdx.x; c < p.chunks;
+         c += (int64_t)gridDim.x * kGatherThreads)
+        for (int d = 0; d < p.n; d++)
+            st32(p.dst[d] + c * 32, v, v);
 }
 
 // ------------------------------------------------------------ launching ----
@@ -687,7 +900,8 @@ class DeviceScope {
 
 // Persistent grid size for `kernel` on `dev`: resident CTAs per SM (at most
 // `max_per_sm`) x SMs.
-fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int max_per_sm, int *grid)
+fsdp_status grid_for(int dev, const void *kernel, int threads, int64_t tiles, int max_per_sm,
+                     int *grid)
 {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo &d = g_dev[dev];
@@ -698,7 +912,7 @@ fsdp_status grid_for(int dev, const void *kernel, int64_t tiles, int max_per_sm,
     auto it = d.blocks_per_sm.find(kernel);
     if (it == d.blocks_per_sm.end()) {
         int nb = 0;
-        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0)) !=
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0)) !=
             cudaSuccess)
             return set_error(FSDP_ECUDA, "cudaOccupancyMaxActiveBlocksPerMultiprocessor: %s",
                              cudaGetErrorString(err));
@@ -728,16 +942,18 @@ void fill_segs(Params &p, const LaunchPlan &plan)
 
 template <typename Params, typename Kernel>
 fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const char *what,
-                int max_per_sm)
+                int max_per_sm, int threads = kThreads)
 {
     int grid = 0;
-    fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), p.total_tiles,
-                              max_per_sm, &grid);
+    fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), threads,
+                              p.total_tiles, max_per_sm, &grid);
     if (st != FSDP_OK)
         return st;
-    kernel<<<grid, kThreads, 0, stream>>>(p);
+    kernel<<<grid, threads, 0, stream>>>(p);
     return check_launch(what);
 }
+
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // One kernel launch of a call over n units: its segments, and for each unit
 // slot k of the launch the caller's unit index units[k]. Slot k's rank r
@@ -840,6 +1056,24 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
     return FSDP_OK;
 }
 
+template <bool kUnits>
+static fsdp_status gather_dispatch(int dev, int R, bool bf16, GatherParams &p, cudaStream_t s)
+{
+    const char *w = "all_gather";
+    const int per = kGatherCtasPerSm, th = kGatherThreads;
+    switch (bf16 ? R : -R) {
+    case 2: return run(dev, all_gather_kernel<2, 2, kUnits>, p, s, w, per, th);
+    case 4: return run(dev, all_gather_kernel<4, 2, kUnits>, p, s, w, per, th);
+    case 8: return run(dev, all_gather_kernel<8, 2, kUnits>, p, s, w, per, th);
+    case -2: return run(dev, all_gather_kernel<2, 4, kUnits>, p, s, w, per, th);
+    case -4: return run(dev, all_gather_kernel<4, 4, kUnits>, p, s, w, per, th);
+    case -8: return run(dev, all_gather_kernel<8, 4, kUnits>, p, s, w, per, th);
+    default:
+        return bf16 ? run(dev, all_gather_kernel<0, 2, kUnits>, p, s, w, per, th)
+                    : run(dev, all_gather_kernel<0, 4, kUnits>, p, s, w, per, th);
+    }
+}
+
 fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void *const *shard,
                               void *const *full_out, void *stream)
 {
@@ -858,46 +1092,42 @@ fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void 
         bind(p.shard, shard, l, L->R);
         bind(p.full, full_out, l, L->R);
         fill_segs(p, l.get());
-        switch (bf16 ? L->R : -L->R) {
-        case 2: st = run(dev, all_gather_kernel<2, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
-        case 4: st = run(dev, all_gather_kernel<4, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
-        case 8: st = run(dev, all_gather_kernel<8, 2>, p, s, "all_gather", kGatherCtasPerSm); break;
-        case -2: st = run(dev, all_gather_kernel<2, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
-        case -4: st = run(dev, all_gather_kernel<4, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
-        case -8: st = run(dev, all_gather_kernel<8, 4>, p, s, "all_gather", kGatherCtasPerSm); break;
-        default:
-            st = bf16 ? run(dev, all_gather_kernel<0, 2>, p, s, "all_gather", kGatherCtasPerSm)
-                      : run(dev, all_gather_kernel<0, 4>, p, s, "all_gather", kGatherCtasPerSm);
-        }
+        p.wide = 1;
+        for (size_t k = 0; k < l.units.size() * L->R; k++)
+            p.wide &= aligned32(p.shard[k]) && aligned32(p.full[k]);
+        st = l.units.size() > 1 ? gather_dispatch<true>(dev, L->R, bf16, p, s)
+                                : gather_dispatch<false>(dev, L->R, bf16, p, s);
         if (st != FSDP_OK)
             return st;
     }
     return FSDP_OK;
 }
 
-template <bool kGradBf16, bool kParamBf16, bool kAccum>
+template <bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
 static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
 {
     const char *w = "rs_adamw";
+    const int per = kRsCtasPerSm;
     switch (R) {
-    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
-    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
-    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
-    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16, kAccum>, p, s, w, kRsCtasPerSm);
+    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
+    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
+    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
+    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
     }
 }
 
-template <bool kAccum>
+// Accumulating launches always hold one unit.
+template <bool kAccum, bool kUnits>
 static fsdp_status rs_dispatch_dtypes(int dev, const fsdp_layout_t *L, RsParams &p, cudaStream_t s)
 {
     const bool gb = L->grad_dtype == FSDP_BF16, pb = L->param_dtype == FSDP_BF16;
     if (gb && pb)
-        return rs_dispatch<true, true, kAccum>(dev, L->R, p, s);
+        return rs_dispatch<true, true, kAccum, kUnits>(dev, L->R, p, s);
     if (gb)
-        return rs_dispatch<true, false, kAccum>(dev, L->R, p, s);
+        return rs_dispatch<true, false, kAccum, kUnits>(dev, L->R, p, s);
     if (pb)
-        return rs_dispatch<false, true, kAccum>(dev, L->R, p, s);
-    return rs_dispatch<false, false, kAccum>(dev, L->R, p, s);
+        return rs_dispatch<false, true, kAccum, kUnits>(dev, L->R, p, s);
+    return rs_dispatch<false, false, kAccum, kUnits>(dev, L->R, p, s);
 }
 
 fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *const *grad,
@@ -925,8 +1155,12 @@ fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *c
         bind(p.pshard, param_shard_out, l, R);
         bind(p.gshard, grad_shard_out, l, R);
         fill_segs(p, l.get());
-        st = acc ? rs_dispatch_dtypes<true>(ds.device(), L, p, s)
-                 : rs_dispatch_dtypes<false>(ds.device(), L, p, s);
+        if (acc)
+            st = rs_dispatch_dtypes<true, false>(ds.device(), L, p, s);
+        else if (l.units.size() > 1)
+            st = rs_dispatch_dtypes<false, true>(ds.device(), L, p, s);
+        else
+            st = rs_dispatch_dtypes<false, false>(ds.device(), L, p, s);
         if (st != FSDP_OK)
             return st;
     }
@@ -1001,9 +1235,11 @@ fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, v
     p.P = L->P;
     p.inv_R = 1.0f / (float)L->R;
     p.total_tiles = (L->P + kTile - 1) / kTile;
+    p.wide = 1;
     for (int r = 0; r < L->R; r++) {
         p.grad[r] = grad[r];
         p.out[r] = out[r];
+        p.wide &= aligned32(out[r]);
     }
     cudaStream_t s = (cudaStream_t)stream;
     const bool gb = L->grad_dtype == FSDP_BF16, ob = out_dtype == FSDP_BF16;
@@ -1015,6 +1251,29 @@ fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, v
     if (ob)
         return ar_dispatch<false, true>(dev, L->R, p, s);
     return ar_dispatch<false, false>(dev, L->R, p, s);
+}
+
+fsdp_status launch_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,
+                                void *stream)
+{
+    DeviceScope ds;
+    fsdp_status st = ds.enter(dst[0]);
+    if (st != FSDP_OK)
+        return st;
+    WriteParams p;
+    memset(&p, 0, sizeof p);
+    p.n = n;
+    p.pattern = pattern;
+    p.chunks = bytes / 32;
+    for (int d = 0; d < n; d++)
+        p.dst[d] = static_cast<unsigned char *>(dst[d]);
+    int grid = 0;
+    const int64_t blocks = (p.chunks + kGatherThreads - 1) / kGatherThreads;
+    if ((st = grid_for(ds.device(), reinterpret_cast<const void *>(write_stream_kernel),
+                       kGatherThreads, blocks, kGatherCtasPerSm, &grid)) != FSDP_OK)
+        return st;
+    write_stream_kernel<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(p);
+    return check_launch("write_stream");
 }
 
 }  // namespace fsdp

@@ -36,13 +36,13 @@
  *    every pointer in it (non-NULL, 16-byte aligned), and that no output
  *    range [p, p + bytes) overlaps any other buffer's range, where bytes is
  *    what the layout says the buffer holds (e.g. P elements of grad_dtype
- *    for a full gradient). It also checks that the first output buffer is
- *    device memory. A failed check returns a negative status, sets the
- *    thread's fsdp_last_error() message and launches nothing. A plain
- *    pointer carries no size, dtype or device, so the library cannot see
- *    that an allocation is too short, holds another dtype or lives on
- *    another GPU: that is the caller's part (the Python binding checks it
- *    on every tensor before the call). No kernel traps or asserts.
+ *    for a full gradient), and that every buffer is device memory of one
+ *    device (cudaPointerGetAttributes). A failed check returns a negative
+ *    status, sets the thread's fsdp_last_error() message and launches
+ *    nothing. A plain pointer carries no size or dtype, so the library
+ *    cannot see that an allocation is too short or holds another dtype:
+ *    that is the caller's part (the Python binding checks both on every
+ *    tensor before the call). No kernel traps or asserts.
  *  - Kernel calls are asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and never synchronise. They run on the device
  *    that owns the first output buffer, which every buffer of the call must
@@ -273,6 +273,16 @@ fsdp_status fsdp_reduce_scatter_adamw_units(int n_units, const fsdp_layout_t *co
                                             void *const *param_shard_out,
                                             float *const *grad_shard_out, const fsdp_adamw_hp *hp,
                                             int64_t step, void *stream);
+
+/* Measurement helper; the pages have no counterpart. Writes the 32-bit
+ * `pattern` over the first `bytes` bytes of each of the n device buffers
+ * dst[0..n) (1 <= n <= FSDP_MAX_RANKS; bytes a multiple of 32; buffers
+ * 32-byte aligned, disjoint, on one device), with the all-gather's store
+ * pattern and grid. Timing it gives the write-only stream ceiling that
+ * bounds the all-gather (which writes R bytes per byte read) and the
+ * all-reduce. Errors: FSDP_EINVAL, FSDP_EALIGN, FSDP_ECUDA. */
+fsdp_status fsdp_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,
+                              void *stream);
 
 /* Message for the last non-OK status returned on the calling thread. */
 const char *fsdp_last_error(void);

@@ -10,8 +10,8 @@ pytestmark = pytest.mark.gpu
 
 
 def test_bench_line_contract(cuda_lib, capsys):
-    bench.main(["--workload", "llama_attn", "--steps", "5", "--warmup", "3", "--no-small",
-                "--no-cpu-baseline", "--e2e-steps", "2"])
+    bench.main(["--workload", "llama_attn", "--steps", "5", "--warmup", "3", "--no-configs",
+                "--no-cpu-baseline"])
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
@@ -30,3 +30,42 @@ def test_bench_line_contract(cuda_lib, capsys):
     for entry in (line["roofline_all_gather"], line["ddp_all_reduce"], line["pack"],
                   *line["grad_accumulation"].values()):
         assert entry["achieved"] > 0
+        assert entry["frac_of_nominal"] < entry["frac"]
+    ceil = line["ceilings"]
+    for key in ("write_only_x_R_gbs", "device_copy_x_R_gbs", "h2d_pinned_gbs", "d2h_pinned_gbs"):
+        assert ceil[key] > 0, key
+    assert "frac_of_write_ceiling" in roof
+    # the step allocates nothing beyond the FSDP2 page's peak-memory terms
+    for sched in ("in_order", "prefetch"):
+        mem = line["peak_memory"][sched]
+        assert abs(mem["measured_bytes"] - mem["formula_bytes"]) <= 65536, mem
+    assert line["peak_memory"]["prefetch"]["M_prefetch"] > 0
+
+
+def test_peak_memory_matches_the_pages_formula(cuda_lib):
+    """Peak device memory of a step of twelve 512/8/2048 blocks (R = 4),
+    in order and with prefetch, equals the FSDP2 page's §01 formula as the
+    oracle states it: the peak of the bytes requested from the allocator
+    (its own block rounding left out) equals the formula to within 64 KB."""
+    import torch
+    from fractions import Fraction
+
+    from fully_sharded_state_gb300 import AdamWHP, synth
+    from oracle import formulas
+
+    wl = synth.WORKLOADS["block12_flat"]
+    shapes = [wl.unit_shapes(u) for u in range(len(wl.units))]
+    got = bench.peak_memory(torch, torch.device("cuda"), shapes, wl.R, "per_param",
+                            AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01))
+    P = wl.unit_numel(0)
+    R = wl.R
+    import oracle
+    S = oracle.layout(oracle.PER_PARAM, R, shapes[0]).shard_numel
+    # sharded state: bf16 shard + fp32 master (b_w = 6), no stored gradient
+    # shard (b_g = 0), AdamW m and v (b_o = 8), for R ranks over 12 units
+    m_shard = 12 * R * formulas.shard_state_bytes(S * R, 6, 0, 8, R)
+    full_unit = R * P * 2
+    for sched, prefetch in (("in_order", 0), ("prefetch", full_unit)):
+        want = formulas.peak_bytes(m_shard, full_unit, prefetch, activations=0, temp=full_unit)
+        assert want == Fraction(got[sched]["formula_bytes"])
+        assert abs(got[sched]["measured_bytes"] - want) <= 65536, (sched, got[sched])

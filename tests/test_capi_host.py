@@ -455,3 +455,16 @@ def test_units_calls_skip_empty_units(lib):
     assert lib.fsdp_all_gather_unflatten_units(2, lay, nul, nul, None) == capi.FSDP_OK
     assert lib.fsdp_reduce_scatter_adamw_units(2, lay, nul, nul, nul, nul, nul, None,
                                                ctypes.byref(_hp()), 1, None) == capi.FSDP_OK
+
+
+def test_write_stream_rejects_bad_arguments(lib):
+    MB = 1 << 20
+    d = _ptrs([BASE, BASE + MB])
+    assert lib.fsdp_write_stream(None, 2, 1024, 0, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_write_stream(d, 0, 1024, 0, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_write_stream(d, 2, 1000, 0, None) == capi.FSDP_EINVAL  # not 32-byte chunks
+    assert lib.fsdp_write_stream(_ptrs([BASE + 16, BASE + MB]), 2, 1024, 0,
+                                 None) == capi.FSDP_EALIGN
+    # overlapping destinations
+    assert lib.fsdp_write_stream(_ptrs([BASE, BASE + 512]), 2, 1024, 0, None) == capi.FSDP_EINVAL
+    assert lib.fsdp_write_stream(d, 2, 0, 0, None) == capi.FSDP_OK

@@ -101,3 +101,82 @@ def test_short_view_is_refused_before_any_write(cuda_lib):
     assert U.step == 0
     torch.cuda.synchronize()
     assert torch.all(blk == 0xA5)
+
+
+def test_host_memory_inputs_are_refused(cuda_lib):
+    """Every buffer must be device memory: pinned host memory passed as a
+    shard (an input) is refused by the C library before any launch."""
+    import ctypes
+    from fully_sharded_state_gb300 import capi
+    U = ShardedUnit([(64, 64)], R=2)
+    full = U.alloc_full()
+    pinned = [torch.empty(U.S, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lib = capi.load()
+    arr_in = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in pinned])
+    arr_out = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in full])
+    st = lib.fsdp_all_gather_unflatten(U.layout.handle, arr_in, arr_out, None)
+    assert st == capi.FSDP_EINVAL
+    assert b"not device memory" in lib.fsdp_last_error()
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("pdt", ["bf16", "f32"])
+def test_sixteen_byte_aligned_buffers(cuda_lib, pdt):
+    """Buffers that are 16-byte but not 32-byte aligned (views 16 bytes into
+    an allocation) take the kernels' 16-byte-vector paths; the results are
+    the oracle's, bit for bit, and equal those of aligned buffers."""
+    import numpy as np
+
+    import oracle
+    from parity import host, to_dev
+    R = 4
+    shapes = [(512, 64), (96, 40), (7, 513)]
+    U = ShardedUnit(shapes, R, "per_param", pdt, "bf16")
+    O = oracle.layout(oracle.PER_PARAM, R, shapes)
+    w = synth.host_normal(5, U.P, 0.02)
+    U.shard_from_full(to_dev(w))
+    masters, p16 = oracle.pack(O, w, with_bf16=pdt == "bf16")
+    tp = torch.bfloat16 if pdt == "bf16" else torch.float32
+
+    def offset_views(n, dtype, count):
+        bufs = [torch.zeros(n + 64, dtype=dtype, device="cuda") for _ in range(count)]
+        return bufs, [b[16 // torch.tensor([], dtype=dtype).element_size():][:n] for b in bufs]
+
+    # shards moved into 16-byte offset views, destinations likewise
+    _, sh = offset_views(U.S, tp, R)
+    for r in range(R):
+        sh[r].copy_(U.gather_sources()[r])
+    _, full = offset_views(U.P, tp, R)
+    assert all(t.data_ptr() % 32 == 16 for t in sh + full)
+    from fully_sharded_state_gb300 import capi
+    capi.fsdp_all_gather_unflatten(U.layout, sh, full)
+    want = oracle.all_gather(O, p16 if pdt == "bf16" else masters)
+    for d in range(R):
+        np.testing.assert_array_equal(host(full[d]).view(np.uint8), want[d].view(np.uint8))
+    # all-reduce into 16-byte offset fp32 outputs equals the aligned result
+    g = [to_dev(x) for x in synth.host_grads(synth.WORKLOADS["block"], 0)[:R]]
+    gP = [x[:U.P].contiguous() for x in g]
+    _, out_off = offset_views(U.P, torch.float32, R)
+    out_al = [torch.empty(U.P, dtype=torch.float32, device="cuda") for _ in range(R)]
+    U.all_reduce(gP, out_off, "f32")
+    U.all_reduce(gP, out_al, "f32")
+    want = oracle.all_reduce([host(x) for x in gP], out_bf16=False)
+    for d in range(R):
+        assert torch.equal(out_off[d].view(torch.int32), out_al[d].view(torch.int32))
+        np.testing.assert_array_equal(host(out_al[d]).view(np.uint32), want[d].view(np.uint32))
+    torch.cuda.synchronize()
+
+
+def test_write_stream_helper_writes_exactly_its_buffers(cuda_lib):
+    """The write-stream measurement helper fills each buffer with its
+    pattern and nothing around it."""
+    from fully_sharded_state_gb300 import capi
+    n, nbytes, guard = 3, 1 << 20, 4096
+    blk = [torch.full((nbytes + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+           for _ in range(n)]
+    dst = [b[guard:guard + nbytes].view(torch.float32) for b in blk]
+    capi.fsdp_write_stream(dst, pattern=0x3F800000)
+    torch.cuda.synchronize()
+    for b, d in zip(blk, dst):
+        assert torch.all(d == 1.0)
+        assert torch.all(b[:guard] == 0xA5) and torch.all(b[guard + nbytes:] == 0xA5)
