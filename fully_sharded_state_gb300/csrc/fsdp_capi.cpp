@@ -44,14 +44,16 @@ bool mul_ok(int64_t a, int64_t b, int64_t *out)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Tiles of one rank piece of `len` elements.
-int64_t tiles_for(int64_t len) { return ceil_div(len, kTile); }
+// Tiles of `tile` elements in one rank piece of `len` elements.
+int64_t tiles_for(int64_t len, int64_t tile) { return ceil_div(len, tile); }
 
 // Split segments into launches of at most kMaxSegsPerLaunch segments, with
 // the tile numbering of each launch starting at 0. `padded` selects the
 // traversal: owned elements only (gather, reduce) or whole shard buffers
-// (pack). Segments without tiles are dropped.
-std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool padded)
+// (pack); `tile` is the kernel's tile length. Segments without tiles are
+// dropped.
+std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool padded,
+                                   int64_t tile)
 {
     std::vector<LaunchPlan> plans;
     LaunchPlan cur;
@@ -59,18 +61,18 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
         int64_t tiles;
         if (s.owner >= 0) {
             // a whole parameter on one rank: tiles over its (padded) length
-            tiles = tiles_for(padded ? s.pad_len : s.numel);
+            tiles = tiles_for(padded ? s.pad_len : s.numel, tile);
             s.tiles_per_rank = tiles;
         } else if (padded) {
-            s.tiles_per_rank = tiles_for(s.pad_len);
+            s.tiles_per_rank = tiles_for(s.pad_len, tile);
             tiles = s.tiles_per_rank * R;
         } else {
             if (s.numel == 0 || s.rank_stride == 0)
                 continue;
-            s.tiles_per_rank = tiles_for(s.rank_stride);
+            s.tiles_per_rank = tiles_for(s.rank_stride, tile);
             int64_t full_ranks = s.numel / s.rank_stride;
             int64_t rest = s.numel - full_ranks * s.rank_stride;
-            tiles = full_ranks * s.tiles_per_rank + tiles_for(rest);
+            tiles = full_ranks * s.tiles_per_rank + tiles_for(rest, tile);
         }
         if (tiles == 0)
             continue;
@@ -420,8 +422,9 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
         delete L;
         return set_error(FSDP_ERANGE, "fsdp_layout: shard buffers too large");
     }
-    L->valid_plans = make_plans(segs, R, false);
-    L->padded_plans = make_plans(segs, R, true);
+    L->valid_plans = make_plans(segs, R, false, kTile);
+    L->gather_plans = make_plans(segs, R, false, kGatherTile);
+    L->padded_plans = make_plans(segs, R, true, kTile);
     *out = L;
     return FSDP_OK;
 }

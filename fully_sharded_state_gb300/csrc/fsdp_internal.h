@@ -15,6 +15,10 @@ namespace fsdp {
 constexpr int kThreads = 256;
 constexpr int kElemsPerThread = 8;
 constexpr int64_t kTile = (int64_t)kThreads * kElemsPerThread;
+// The all-gather's threads own 16 elements each (one 32-byte vector of bf16),
+// so its tiles are twice as long.
+constexpr int kGatherEPT = 16;
+constexpr int64_t kGatherTile = (int64_t)kThreads * kGatherEPT;
 // Segment descriptors travel in the kernel parameter block; larger units are
 // split into several launches.
 constexpr int kMaxSegsPerLaunch = 256;
@@ -94,6 +98,7 @@ struct fsdp_layout_s {
     std::vector<int64_t> owner;  // ZERO3: owner rank of each parameter
     int64_t P;            // full numel
     int64_t shard_numel;  // per-rank shard buffer numel
-    std::vector<fsdp::LaunchPlan> valid_plans;   // tiles over owned elements (gather, reduce)
-    std::vector<fsdp::LaunchPlan> padded_plans;  // tiles over whole shard buffers (pack)
+    std::vector<fsdp::LaunchPlan> valid_plans;   // kTile tiles over owned elements (reduce)
+    std::vector<fsdp::LaunchPlan> gather_plans;  // kGatherTile tiles over owned elements
+    std::vector<fsdp::LaunchPlan> padded_plans;  // kTile tiles over whole shard buffers (pack)
 };

@@ -4,17 +4,18 @@
 // no tensor-core work. The layout-driven kernels (pack, all-gather, fused
 // reduce-scatter + AdamW) share one work decomposition: a launch covers up to
 // kMaxSegsPerLaunch segments (parameters, one FlatParameter, or ZeRO-3 tensors
-// with their owner ranks); each segment's rank pieces are cut into tiles of
-// kTile elements; a persistent grid (a few CTAs per SM) walks the tiles in
-// order, so at any moment the grid touches one contiguous window of every
-// buffer. Each thread owns 8 consecutive elements of a tile: one 16-byte
+// with their owner ranks, from one unit or several); each segment's rank
+// pieces are cut into tiles (kTile elements; kGatherTile for the gather); a
+// persistent grid (a few CTAs per SM) walks the tiles in order, so at any
+// moment the grid touches one contiguous window of every buffer. A thread
+// owns 8 consecutive elements of a tile (16 in the gather): one 16-byte
 // vector per bf16 stream, two per fp32 stream. Tiles whose start is not
-// 8-element aligned in both the full and the shard buffer (ragged FSDP1
-// boundaries, odd row widths) take a scalar path with the same per-element
-// arithmetic. The all-reduce and gradient-accumulation kernels tile the flat
-// unit index the same way.
+// aligned in both the full and the shard buffer (ragged FSDP1 boundaries,
+// odd row widths) take a scalar path with the same per-element arithmetic.
+// The all-reduce and gradient-accumulation kernels tile the flat unit index
+// the same way.
 //
-// Segment descriptors and the R per-rank pointers travel in the kernel
+// Segment descriptors and the per-rank pointers travel in the kernel
 // parameter block (__grid_constant__), so the kernels need no device memory
 // beyond the caller's buffers.
 #include <cuda_bf16.h>
@@ -39,8 +40,9 @@ constexpr int kMaxR = FSDP_MAX_RANKS;
 // Fewer CTAs, each streaming its tiles in order, keep a narrower window of
 // every buffer open at once; past these points HBM does not go faster.
 constexpr int kRsCtasPerSm = 3;
-// all-gather: CTAs of kGatherThreads (128) threads.
-constexpr int kGatherCtasPerSm = 2;
+// all-gather (256 threads, 16 elements per thread): 1/SM 0.613 ms,
+// 2/SM 0.668 ms, 3/SM 0.667 ms.
+constexpr int kGatherCtasPerSm = 1;
 // pack (set-up): 1/SM 0.810, 2/SM 0.482, 3/SM 0.404, 4/SM 0.356, 6/SM
 // 0.421, 8/SM 0.418 ms.
 constexpr int kPackCtasPerSm = 4;
@@ -95,6 +97,8 @@ struct Tile {
     int64_t nvalid;  // padded traversal: elements of the tile that the rank owns
 };
 
+// kT: the kernel's tile length.
+template <int64_t kT>
 __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool padded)
 {
     int lo = 0, hi = nseg - 1;
@@ -112,12 +116,12 @@ __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool
     if (s.owner >= 0) {  // a whole parameter on its owner rank
         r = (int)s.owner;
         first_of_rank = 0;
-        off = tl * kTile;
+        off = tl * kT;
         owned = s.numel;
     } else {
         r = (int)(tl / s.tiles_per_rank);
         first_of_rank = r;
-        off = (tl - (int64_t)r * s.tiles_per_rank) * kTile;
+        off = (tl - (int64_t)r * s.tiles_per_rank) * kT;
         owned = s.numel - (int64_t)r * s.rank_stride;
         owned = owned < 0 ? 0 : (owned > s.rank_stride ? s.rank_stride : owned);
     }
@@ -127,7 +131,7 @@ __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool
     T.base = s.base;
     T.fbase = s.full_off + (int64_t)first_of_rank * s.rank_stride + off;
     T.sbase = s.shard_off + off;
-    T.len = piece - off < kTile ? piece - off : kTile;
+    T.len = piece - off < kT ? piece - off : kT;
     int64_t nv = owned - off;
     T.nvalid = nv < 0 ? 0 : (nv > T.len ? T.len : nv);
     return T;
@@ -169,7 +173,7 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ PackParams p)
 {
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const Tile T = locate(p.seg, p.nseg, t, true);  // one unit: base 0
+        const Tile T = locate<kTile>(p.seg, p.nseg, t, true);  // one unit: base 0
         float *dst = p.master[T.rank] + T.sbase;
         uint16_t *dst16 = kBf16 ? p.pshard[T.rank] + T.sbase : nullptr;
         const float *src = p.full + T.fbase;
@@ -226,19 +230,28 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
 // ----------------------------------------------------- all-gather ----------
 //
 // The gather writes R bytes for every byte it reads, so its store pattern
-// sets its speed. It runs 128-thread CTAs, each thread owning 16 consecutive
-// elements of a tile: with 32-byte aligned buffers every store instruction
-// writes whole 32-byte sectors (one 32-byte vector per destination for
-// bf16, two for fp32). Two 16-byte halves of one sector written by separate
-// instructions cost about 1.8x the DRAM time of whole-sector writes on GB300
-// (a write-only stream of 8 fp32 buffers: 3.7 TB/s with 16-byte halves,
-// 6.5 TB/s with 32-byte stores). Tiles that are only 16-byte aligned use
-// 16-byte vectors laid out so that a warp's instruction still covers 512
-// contiguous bytes; other tiles copy element by element.
+// sets its speed. Each thread owns 16 consecutive elements of a
+// kGatherTile-element tile: with 32-byte aligned buffers every store
+// instruction writes whole 32-byte sectors (one 32-byte vector per
+// destination for bf16, two for fp32). Two 16-byte halves of one sector
+// written by separate instructions cost about 1.8x the DRAM time of
+// whole-sector writes on GB300 (a write-only stream of 8 fp32 buffers: 3.7
+// TB/s with 16-byte halves, 6.5 TB/s with 32-byte stores). Tiles that are
+// only 16-byte aligned use 16-byte vectors laid out so that a warp's
+// instruction still covers 512 contiguous bytes; other tiles copy element
+// by element.
+//
+// Measured interplay on GB300 (Llama unit, R = 8, gather then reduce-scatter
+// as in a step): after this gather the reduce-scatter takes 1.376 ms, after
+// a gather whose threads store 16 bytes each (512 bytes per warp
+// instruction) 1.327 ms, with identical reduce-scatter code and identical
+// placement of its CTAs on the SMs; the 16-byte gather itself takes
+// 0.627-0.666 ms against 0.613 ms here. The sum is about 1 % in favour of
+// the 16-byte gather; this one is kept because it alone holds the gather
+// above 80 % of the nominal HBM bandwidth.
 
-constexpr int kGatherThreads = 128;
-constexpr int kGatherEPT = 16;
-static_assert(kGatherThreads * kGatherEPT == kTile, "a gather CTA covers one tile");
+constexpr int kGatherThreads = kThreads;
+static_assert(kGatherThreads * kGatherEPT == kGatherTile, "a gather CTA covers one tile");
 
 template <int kEB> struct ElemOf;
 template <> struct ElemOf<2> { using T = unsigned short; };
@@ -269,7 +282,7 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
     constexpr int kV = 16 / kEB;                     // elements per 16-byte vector
     constexpr int kW = 32 / kEB;                     // elements per 32-byte vector
     constexpr int kWide = kGatherEPT / kW;           // 32-byte vectors per thread
-    constexpr int kNarrow = kTile / (kGatherThreads * kV);  // 16-byte vectors per thread
+    constexpr int kNarrow = kGatherTile / (kGatherThreads * kV);  // 16-byte vectors per thread
     const int n = RC > 0 ? RC : R;
     const E *src = reinterpret_cast<const E *>(p.shard[T.base + T.rank]) + T.sbase;
     // destination pointers in registers when R is known at compile time
@@ -332,13 +345,21 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
         }
         return;
     }
-#pragma unroll 4
-    for (int k = 0; k < kGatherEPT; k++) {
-        const int64_t q = tid + (int64_t)k * kGatherThreads;
-        if (q < T.len) {
-            const E x = src[q];
-            for (int d = 0; d < n; d++)
-                reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
+    // element by element, four loads of a thread before their stores
+#pragma unroll 1
+    for (int k0 = 0; k0 < kGatherEPT; k0 += 4) {
+        E x[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int64_t q = tid + (int64_t)(k0 + k) * kGatherThreads;
+            x[k] = q < T.len ? src[q] : E(0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int64_t q = tid + (int64_t)(k0 + k) * kGatherThreads;
+            if (q < T.len)
+                for (int d = 0; d < n; d++)
+                    reinterpret_cast<E *>(full[d])[T.fbase + q] = x[k];
         }
     }
 }
@@ -352,7 +373,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 {
     const int R = RC > 0 ? RC : p.R;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        Tile T = locate(p.seg, p.nseg, t, false);
+        Tile T = locate<kGatherTile>(p.seg, p.nseg, t, false);
         if (!kUnits)
             T.base = 0;
         gather_tile<RC, kEB>(p, R, T);
@@ -434,6 +455,52 @@ __device__ __forceinline__ void rs_adamw_scalar(const RankPtrs &b, const AdamSca
         b.pshard[s] = f32_to_bf16_bits(o.w);
     if (b.gshard)
         b.gshard[s] = g;
+}
+
+// Two elements of a misaligned tile at once, with R known at compile time:
+// every load of both comes before any store, so their latencies overlap
+// (the compiler cannot move loads above the stores, which it must assume
+// may alias). Element 1 is skipped when has1 is false.
+template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum>
+__device__ __forceinline__ void rs_adamw_scalar_pair(const RankPtrs &b, const AdamScalars &c,
+                                                     int64_t j0, int64_t s0, int64_t j1,
+                                                     int64_t s1, bool has1)
+{
+    float g0[RC], g1[RC];
+#pragma unroll
+    for (int q = 0; q < RC; q++) {
+        g0[q] = rank_grad<kGradBf16, kAccum>(b, q, j0);
+        g1[q] = has1 ? rank_grad<kGradBf16, kAccum>(b, q, j1) : 0.0f;
+    }
+    const float w0 = b.master[s0], m0 = b.m[s0], v0 = b.v[s0];
+    const float w1 = has1 ? b.master[s1] : 0.0f, m1 = has1 ? b.m[s1] : 0.0f,
+                v1 = has1 ? b.v[s1] : 0.0f;
+    float a0 = g0[0], a1 = g1[0];
+#pragma unroll
+    for (int q = 1; q < RC; q++) {
+        a0 = __fadd_rn(a0, g0[q]);
+        a1 = __fadd_rn(a1, g1[q]);
+    }
+    a0 = __fmul_rn(a0, c.inv_R);
+    a1 = __fmul_rn(a1, c.inv_R);
+    const AdamOut o0 = adamw_elem(c, a0, w0, m0, v0);
+    b.master[s0] = o0.w;
+    b.m[s0] = o0.m;
+    b.v[s0] = o0.v;
+    if (kParamBf16)
+        b.pshard[s0] = f32_to_bf16_bits(o0.w);
+    if (b.gshard)
+        b.gshard[s0] = a0;
+    if (has1) {
+        const AdamOut o1 = adamw_elem(c, a1, w1, m1, v1);
+        b.master[s1] = o1.w;
+        b.m[s1] = o1.m;
+        b.v[s1] = o1.v;
+        if (kParamBf16)
+            b.pshard[s1] = f32_to_bf16_bits(o1.w);
+        if (b.gshard)
+            b.gshard[s1] = a1;
+    }
 }
 
 __device__ __forceinline__ void unpack_bf16x8(uint4 x, float out[8])
@@ -544,12 +611,23 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
         b.grad = gl;
     }
     if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
+        if constexpr (RC > 0) {
 #pragma unroll 1
-        for (int k = 0; k < kElemsPerThread; k++) {
-            int64_t e = threadIdx.x + (int64_t)k * kThreads;
-            if (e < T.len)
-                rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(b, p.c, R, T.fbase + e,
-                                                               T.sbase + e);
+            for (int k = 0; k < kElemsPerThread; k += 2) {
+                const int64_t e0 = threadIdx.x + (int64_t)k * kThreads, e1 = e0 + kThreads;
+                if (e0 < T.len)
+                    rs_adamw_scalar_pair<RC, kGradBf16, kParamBf16, kAccum>(
+                        b, p.c, T.fbase + e0, T.sbase + e0, T.fbase + e1, T.sbase + e1,
+                        e1 < T.len);
+            }
+        } else {
+#pragma unroll 1
+            for (int k = 0; k < kElemsPerThread; k++) {
+                const int64_t e = threadIdx.x + (int64_t)k * kThreads;
+                if (e < T.len)
+                    rs_adamw_scalar<kGradBf16, kParamBf16, kAccum>(b, p.c, R, T.fbase + e,
+                                                                   T.sbase + e);
+            }
         }
         return;
     }
@@ -607,7 +685,7 @@ __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constan
 {
     const int R = RC > 0 ? RC : p.R;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        Tile T = locate(p.seg, p.nseg, t, false);
+        Tile T = locate<kTile>(p.seg, p.nseg, t, false);
         if (!kUnits)
             T.base = 0;
         rs_adamw_tile<RC, kGradBf16, kParamBf16, kAccum>(p, R, T);
@@ -965,14 +1043,17 @@ struct Launch {
     const LaunchPlan &get() const { return plan ? *plan : merged; }
 };
 
+// Which of a layout's plans a kernel walks.
+using Plans = std::vector<LaunchPlan> fsdp_layout_s::*;
+
 // The launches of a call over n layouts sharing R: consecutive units share
 // a launch while the launch holds at most kMaxSegsPerLaunch segments and
 // kMaxR pointers per array. One unit takes its layout's own plans.
-std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, bool padded)
+std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, Plans plans)
 {
     std::vector<Launch> out;
     if (n == 1) {
-        for (const LaunchPlan &pl : padded ? Ls[0]->padded_plans : Ls[0]->valid_plans) {
+        for (const LaunchPlan &pl : Ls[0]->*plans) {
             out.emplace_back();
             out.back().plan = &pl;
             out.back().units.push_back(0);
@@ -983,7 +1064,7 @@ std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, bool pa
     const int max_units = kMaxR / R;
     Launch cur;
     for (int u = 0; u < n; u++) {
-        for (const LaunchPlan &pl : padded ? Ls[u]->padded_plans : Ls[u]->valid_plans) {
+        for (const LaunchPlan &pl : Ls[u]->*plans) {
             const bool has_slot = !cur.units.empty() && cur.units.back() == u;
             if ((!has_slot && (int)cur.units.size() == max_units) ||
                 cur.merged.segs.size() + pl.segs.size() > (size_t)kMaxSegsPerLaunch) {
@@ -1041,7 +1122,7 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
     memset(&p, 0, sizeof p);
     p.full = full;
     p.R = L->R;
-    for (const Launch &l : plan_launches(1, &L, true)) {
+    for (const Launch &l : plan_launches(1, &L, &fsdp_layout_s::padded_plans)) {
         bind(p.master, master, l, L->R);
         bind(p.pshard, param_shard, l, L->R);
         fill_segs(p, l.get());
@@ -1088,7 +1169,7 @@ fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void 
     p.R = L->R;
     cudaStream_t s = (cudaStream_t)stream;
     const bool bf16 = L->param_dtype == FSDP_BF16;
-    for (const Launch &l : plan_launches(n, Ls, false)) {
+    for (const Launch &l : plan_launches(n, Ls, &fsdp_layout_s::gather_plans)) {
         bind(p.shard, shard, l, L->R);
         bind(p.full, full_out, l, L->R);
         fill_segs(p, l.get());
@@ -1146,7 +1227,7 @@ fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *c
     p.R = R;
     p.c = c;
     cudaStream_t s = (cudaStream_t)stream;
-    for (const Launch &l : plan_launches(n, Ls, false)) {
+    for (const Launch &l : plan_launches(n, Ls, &fsdp_layout_s::valid_plans)) {
         bind(p.grad, grad, l, R);
         bind(p.acc, acc, l, R);
         bind(p.master, master, l, R);
