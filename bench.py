@@ -712,6 +712,24 @@ def run_ours(args):
             "gpu_launches_per_step": 2 * len(units), "calls": "plain per-unit calls",
             "note": "the headline workload: see value and roofline"}} \
             if args.workload == "llama4" else {}
+        if configs:
+            # the same four units through the prepared multi-unit calls
+            from fully_sharded_state_gb300 import (prepare_all_gather_units,
+                                                   prepare_reduce_scatter_adamw_units)
+            fulls_u = [[f[:U.P] for f in full] if k == 0 else
+                       [torch.empty(U.P, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+                       for k, U in enumerate(units)]
+            ag_call = prepare_all_gather_units(units, fulls_u)
+            rs_call = prepare_reduce_scatter_adamw_units(units, grads)
+            ms_u = timed_back_to_back(torch, stream, lambda: (ag_call(stream=stream),
+                                                              rs_call(hp, stream=stream)), n=20)
+            gbs_u = step_bytes / (ms_u * 1e-3) / 1e9
+            configs["llama4"]["all_units_per_call"] = {
+                "ms_per_step": round(ms_u, 4), "achieved": round(gbs_u, 1),
+                "frac": round(gbs_u / peak, 4), "gpu_launches_per_step": 2,
+                "calls": "prepared multi-unit calls (all four gathers, then all four "
+                         "reduce-scatters)"}
+            del ag_call, rs_call, fulls_u
         for name in ("toy", "block", "block12_flat", "ragged"):
             configs[name] = config_entry(torch, dev, stream, name, hp, peak, peak_src)
 
