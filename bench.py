@@ -530,13 +530,33 @@ def config_entry(torch, dev, stream, name, hp, peak, peak_src):
 
     ms = timed_back_to_back(torch, stream, step)
     gbs = (ag + rs) / (ms * 1e-3) / 1e9
+    # each kernel on its own, every unit once per pass
+    ms_ag = timed_back_to_back(torch, stream, lambda: [U.all_gather(fulls[k], stream=stream)
+                                                       for k, U in enumerate(units)])
+    ms_rs = timed_back_to_back(torch, stream, lambda: [U.reduce_scatter_adamw(grads[k], hp,
+                                                                              stream=stream)
+                                                       for k, U in enumerate(units)])
+    kernels = {name: {"ms": round(t, 4), "algorithmic_bytes": int(nb),
+                      "achieved": round(nb / (t * 1e-3) / 1e9, 1),
+                      "frac": round(nb / (t * 1e-3) / 1e9 / peak, 4)}
+               for name, t, nb in (("all_gather", ms_ag, ag), ("rs_adamw", ms_rs, rs))}
     e = {"workload": name, "cfg": wl.cfg, "units": len(units), "params_per_unit": units[0].P,
          "R": R, "mode": wl.mode, "dtypes": f"{wl.param_dtype} params / {wl.grad_dtype} grads",
          "algorithmic_bytes_per_step": int(ag + rs), "distinct_bytes": int(distinct),
          "l2_resident": bool(distinct < l2), "ms_per_step": round(ms, 4),
          "achieved": round(gbs, 1), "unit": UNIT, "frac": round(gbs / peak, 4),
          "peak_source": peak_src, "gpu_launches_per_step": 2 * len(units),
-         "calls": "plain per-unit calls"}
+         "calls": "plain per-unit calls", "per_kernel": kernels}
+    if len(units) == 1:
+        U, g, f = units[0], grads[0], fulls[0]
+        ag1, rs1 = U.prepare_all_gather(f), U.prepare_reduce_scatter_adamw(g)
+        ms_p = timed_back_to_back(torch, stream, lambda: (ag1(stream=stream),
+                                                          rs1(hp, stream=stream)))
+        gbs_p = (ag + rs) / (ms_p * 1e-3) / 1e9
+        e["prepared_calls"] = {"ms_per_step": round(ms_p, 4), "achieved": round(gbs_p, 1),
+                               "frac": round(gbs_p / peak, 4), "gpu_launches_per_step": 2,
+                               "calls": "prepared per-unit calls"}
+        del ag1, rs1
     if len(units) > 1:
         ag_call = prepare_all_gather_units(units, fulls)
         rs_call = prepare_reduce_scatter_adamw_units(units, grads)

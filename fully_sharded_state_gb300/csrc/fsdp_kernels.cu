@@ -274,9 +274,12 @@ __device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
 // One all-gather tile: the tile's shard elements go to the same place of
 // every destination's full buffer. kEB = element bytes (2 bf16, 4 fp32); the
 // copy is bitwise. PP is any parameter block with `shard`, `full` and `wide`
-// (1 when every shard and full pointer of the launch is 32-byte aligned).
+// (1 when every shard and full pointer of the launch is 32-byte aligned);
+// `stage` is the CTA's shared buffer of kGatherTile elements. Every thread of
+// the CTA calls this with the same tile.
 template <int RC, int kEB, class PP>
-__device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
+__device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T,
+                                            unsigned char *stage)
 {
     using E = typename ElemOf<kEB>::T;
     constexpr int kV = 16 / kEB;                     // elements per 16-byte vector
@@ -345,6 +348,43 @@ __device__ __forceinline__ void gather_tile(const PP &p, int R, const Tile &T)
         }
         return;
     }
+    if ((T.sbase & (kV - 1)) == 0) {
+        // Only the full side is misaligned (odd row widths, ragged FlatParameter
+        // boundaries; shard segments start aligned): stage the tile's shard
+        // elements in shared memory with aligned 16-byte loads, then write
+        // every destination in aligned 16-byte vectors read from the stage at
+        // the shifted offset; the few elements before the first and after the
+        // last aligned destination vector go one by one.
+        E *sE = reinterpret_cast<E *>(stage);
+        const int64_t nvec = T.len / kV;
+        for (int64_t v = tid; v < nvec; v += kGatherThreads)
+            reinterpret_cast<uint4 *>(stage)[v] = ld_stream(src + v * kV);
+        for (int64_t q = nvec * kV + tid; q < T.len; q += kGatherThreads)
+            sE[q] = src[q];
+        __syncthreads();
+        const int64_t head = (kV - (T.fbase & (kV - 1))) & (kV - 1);
+        const int64_t body = T.len > head ? (T.len - head) / kV : 0;
+        for (int64_t v = tid; v < body; v += kGatherThreads) {
+            const int64_t q0 = head + v * kV;
+            uint4 x;
+            E *xe = reinterpret_cast<E *>(&x);
+#pragma unroll
+            for (int i = 0; i < kV; i++)
+                xe[i] = sE[q0 + i];
+#pragma unroll 8
+            for (int d = 0; d < n; d++)
+                st_stream(reinterpret_cast<E *>(full[d]) + T.fbase + q0, x);
+        }
+        for (int64_t q = tid; q < T.len; q += kGatherThreads) {
+            if (q >= head && q < head + body * kV)
+                continue;
+            const E x = sE[q];
+            for (int d = 0; d < n; d++)
+                reinterpret_cast<E *>(full[d])[T.fbase + q] = x;
+        }
+        __syncthreads();  // the stage is free for the next tile
+        return;
+    }
     // element by element, four loads of a thread before their stores
 #pragma unroll 1
     for (int k0 = 0; k0 < kGatherEPT; k0 += 4) {
@@ -371,12 +411,14 @@ template <int RC, int kEB, bool kUnits>
 __global__ void __launch_bounds__(kGatherThreads)
     all_gather_kernel(const __grid_constant__ GatherParams p)
 {
+    // one tile's shard elements, for tiles whose full side is misaligned
+    __shared__ __align__(16) unsigned char stage[kGatherTile * kEB];
     const int R = RC > 0 ? RC : p.R;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         Tile T = locate<kGatherTile>(p.seg, p.nseg, t, false);
         if (!kUnits)
             T.base = 0;
-        gather_tile<RC, kEB>(p, R, T);
+        gather_tile<RC, kEB>(p, R, T, stage);
     }
 }
 

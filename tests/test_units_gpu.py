@@ -180,3 +180,35 @@ def test_write_stream_helper_writes_exactly_its_buffers(cuda_lib):
     for b, d in zip(blk, dst):
         assert torch.all(d == 1.0)
         assert torch.all(b[:guard] == 0xA5) and torch.all(b[guard + nbytes:] == 0xA5)
+
+
+def test_prepared_calls_equal_plain_calls(cuda_lib):
+    """A prepared call (arguments checked and marshalled once) gives the same
+    bits as the plain call, step after step, and keeps its tensors alive."""
+    import gc
+    shapes = [(300, 64), (17, 9), (64,)]
+    hp = AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    A = ShardedUnit(shapes, 4)
+    B = ShardedUnit(shapes, 4)
+    w = torch.randn(A.P, device="cuda") * 0.02
+    A.shard_from_full(w)
+    B.shard_from_full(w)
+    grads = [(torch.randn(A.P, device="cuda") * 1e-3).to(torch.bfloat16) for _ in range(4)]
+    fa, fb = A.alloc_full(), B.alloc_full()
+    gather = A.prepare_all_gather(fa)
+    step = A.prepare_reduce_scatter_adamw([g.clone() for g in grads])
+    del fa
+    gc.collect()
+    for _ in range(3):
+        gather()
+        step(hp)
+        B.all_gather(fb)
+        B.reduce_scatter_adamw(grads, hp)
+    gather()
+    B.all_gather(fb)
+    torch.cuda.synchronize()
+    assert A.step == B.step == 3
+    held = gather._tensors[2]  # the prepared call's own reference to its outputs
+    for r in range(4):
+        assert torch.equal(A.master[r].view(torch.int32), B.master[r].view(torch.int32))
+        assert torch.equal(held[r].view(torch.int16), fb[r].view(torch.int16))
