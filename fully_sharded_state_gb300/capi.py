@@ -212,8 +212,9 @@ class _Args:
     checking each tensor against what the layout says it must hold: the
     count of tensors, a CUDA tensor on the call's one device, contiguous,
     the dtype, and at least the number of elements the kernels touch. The
-    C library can only check pointers (NULL, alignment, overlap), so these
-    checks keep a short or mistyped tensor from reaching a kernel."""
+    C library can only check pointers (NULL, alignment, overlap, device
+    memory of one device), so these checks keep a short or mistyped tensor
+    from reaching a kernel."""
 
     def __init__(self):
         self.device = None
