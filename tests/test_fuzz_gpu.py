@@ -87,3 +87,21 @@ def test_two_threads_two_streams(cuda_lib):
     for t in ts:
         t.join()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("k", range(12))
+def test_random_units_per_call(cuda_lib, k):
+    """Random groups of units through the multi-unit calls: 1 to 24 units
+    sharing R and dtypes, each with its own shapes and layout mode, so the
+    launches split by segment count and by pointer count; every unit is
+    compared with the oracle."""
+    from parity import run_units_case
+    rng = np.random.default_rng(4000 + k)
+    first = _random_case(rng, 1000 + k)
+    cases = [first]
+    for u in range(int(rng.integers(0, 24))):
+        c = _random_case(rng, 1100 + 37 * k + u)
+        c.R, c.param_dtype, c.grad_dtype = first.R, first.param_dtype, first.grad_dtype
+        c.hp = first.hp
+        cases.append(c)
+    run_units_case(cases, step=int(rng.integers(1, 4)))
