@@ -53,11 +53,22 @@ int64_t tiles_for(int64_t len, int64_t tile) { return ceil_div(len, tile); }
 // (pack); `tile` is the kernel's tile length. Segments without tiles are
 // dropped.
 std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool padded,
-                                   int64_t tile)
+                                   int64_t tile, int64_t align)
 {
     std::vector<LaunchPlan> plans;
     LaunchPlan cur;
     for (Seg s : segs) {
+        // owned elements and those in aligned rank pieces (see LaunchPlan)
+        int64_t elems = 0, aligned = 0;
+        const int pieces = s.owner >= 0 ? 1 : R;
+        for (int r = 0; r < pieces; r++) {
+            int64_t n = s.owner >= 0 ? s.numel : s.numel - (int64_t)r * s.rank_stride;
+            n = n < 0 ? 0 : (s.owner < 0 && n > s.rank_stride ? s.rank_stride : n);
+            const int64_t start = s.full_off + (s.owner >= 0 ? 0 : (int64_t)r * s.rank_stride);
+            elems += n;
+            if (start % align == 0 && s.shard_off % align == 0)
+                aligned += n;
+        }
         int64_t tiles;
         if (s.owner >= 0) {
             // a whole parameter on one rank: tiles over its (padded) length
@@ -82,6 +93,8 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
         }
         s.tile_begin = cur.total_tiles;
         cur.total_tiles += tiles;
+        cur.elems += elems;
+        cur.aligned_elems += aligned;
         cur.segs.push_back(s);
     }
     if (!cur.segs.empty())
@@ -422,9 +435,10 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
         delete L;
         return set_error(FSDP_ERANGE, "fsdp_layout: shard buffers too large");
     }
-    L->valid_plans = make_plans(segs, R, false, kTile);
-    L->gather_plans = make_plans(segs, R, false, kGatherTile);
-    L->padded_plans = make_plans(segs, R, true, kTile);
+    const int64_t align = 32 / esize(param_dtype);
+    L->valid_plans = make_plans(segs, R, false, kTile, align);
+    L->gather_plans = make_plans(segs, R, false, kGatherTile, align);
+    L->padded_plans = make_plans(segs, R, true, kTile, align);
     *out = L;
     return FSDP_OK;
 }

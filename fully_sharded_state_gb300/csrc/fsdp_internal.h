@@ -41,10 +41,14 @@ struct Seg {
                              // pointer arrays: rank r's buffer is entry base + r
 };
 
-// The segments of one launch and its tile count.
+// The segments of one launch and its tile count. elems: the elements its
+// tiles cover; aligned_elems: those in rank pieces whose full and shard
+// starts are both 32-byte aligned (the all-gather's vector paths need it).
 struct LaunchPlan {
     std::vector<Seg> segs;
     int64_t total_tiles = 0;
+    int64_t elems = 0;
+    int64_t aligned_elems = 0;
 };
 
 // AdamW scalars, formed on the host in double and rounded once to fp32.

@@ -41,8 +41,13 @@ constexpr int kMaxR = FSDP_MAX_RANKS;
 // every buffer open at once; past these points HBM does not go faster.
 constexpr int kRsCtasPerSm = 3;
 // all-gather (256 threads, 16 elements per thread): 1/SM 0.613 ms,
-// 2/SM 0.668 ms, 3/SM 0.667 ms.
+// 2/SM 0.668 ms, 3/SM 0.667 ms on a Llama unit, whose tiles are full and
+// aligned. A launch whose elements mostly sit in misaligned or partial tiles
+// (the ragged fp32 workload: 2 % aligned, tiles 86 % full) runs faster with
+// more CTAs to overlap their latencies: 1/SM 0.067 ms, 2/SM 0.053, 4/SM
+// 0.051, 8/SM 0.052.
 constexpr int kGatherCtasPerSm = 1;
+constexpr int kGatherCtasPerSmIrregular = 4;
 // pack (set-up): 1/SM 0.810, 2/SM 0.482, 3/SM 0.404, 4/SM 0.356, 6/SM
 // 0.421, 8/SM 0.418 ms.
 constexpr int kPackCtasPerSm = 4;
@@ -1122,6 +1127,8 @@ std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, Plans p
                 cur.merged.segs.push_back(s);
             }
             cur.merged.total_tiles += pl.total_tiles;
+            cur.merged.elems += pl.elems;
+            cur.merged.aligned_elems += pl.aligned_elems;
         }
     }
     if (!cur.units.empty())
@@ -1180,10 +1187,11 @@ fsdp_status launch_pack(const fsdp_layout_t *L, const float *full, void *const *
 }
 
 template <bool kUnits>
-static fsdp_status gather_dispatch(int dev, int R, bool bf16, GatherParams &p, cudaStream_t s)
+static fsdp_status gather_dispatch(int dev, int R, bool bf16, GatherParams &p, cudaStream_t s,
+                                   int per)
 {
     const char *w = "all_gather";
-    const int per = kGatherCtasPerSm, th = kGatherThreads;
+    const int th = kGatherThreads;
     switch (bf16 ? R : -R) {
     case 2: return run(dev, all_gather_kernel<2, 2, kUnits>, p, s, w, per, th);
     case 4: return run(dev, all_gather_kernel<4, 2, kUnits>, p, s, w, per, th);
@@ -1218,8 +1226,14 @@ fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void 
         p.wide = 1;
         for (size_t k = 0; k < l.units.size() * L->R; k++)
             p.wide &= aligned32(p.shard[k]) && aligned32(p.full[k]);
-        st = l.units.size() > 1 ? gather_dispatch<true>(dev, L->R, bf16, p, s)
-                                : gather_dispatch<false>(dev, L->R, bf16, p, s);
+        // irregular: under half the elements in aligned rank pieces, or the
+        // tiles under three quarters full on average
+        const LaunchPlan &pl = l.get();
+        const bool irregular = 2 * pl.aligned_elems < pl.elems ||
+                               4 * pl.elems < 3 * pl.total_tiles * kGatherTile;
+        const int per = irregular ? kGatherCtasPerSmIrregular : kGatherCtasPerSm;
+        st = l.units.size() > 1 ? gather_dispatch<true>(dev, L->R, bf16, p, s, per)
+                                : gather_dispatch<false>(dev, L->R, bf16, p, s, per);
         if (st != FSDP_OK)
             return st;
     }
