@@ -74,6 +74,27 @@ def all_gather_bytes(P: int, R: int, param_b: int = 2) -> int:
     return P * param_b * (1 + R)
 
 
+def rs_kernel_name(shapes, R: int, grad_b: int, sms: int) -> str:
+    """The reduce-scatter + AdamW kernel the library launches for one FSDP2
+    unit: the staged one (gradient slices by cp.async.bulk) when the R
+    gradient streams carry at least 8 bytes per element, a stage (R slices of
+    a 2,048-element tile) fits in 32 KB and the launch has at least 32 tiles
+    per staged thread block (2 per SM); the register one otherwise."""
+    tiles = 0
+    for s in shapes:
+        inner = 1
+        for x in s[1:]:
+            inner *= x
+        rows = -(-s[0] // R)
+        for r in range(R):
+            n = max(0, min(rows, s[0] - r * rows)) * inner
+            tiles += -(-n // 2048)
+    if (R in (2, 4, 8) and R * grad_b >= 8 and R * 2048 * grad_b <= 32 * 1024
+            and tiles >= 32 * 2 * sms):
+        return "rs_adamw_staged_kernel"
+    return "rs_adamw_kernel"
+
+
 # ------------------------------------------------------------------ helpers --
 
 def measured_peak():
@@ -682,7 +703,9 @@ def run_ours(args):
                               profiled_traffic(traffic_key, args.workload) if traffic_key
                               else None, ceilings)
 
-    roofline = entry("rs_adamw_kernel (fused reduce-scatter + AdamW)", rs_bytes / len(units),
+    rs_name = rs_kernel_name(units[0].shapes, R, 2,
+                             torch.cuda.get_device_properties(dev).multi_processor_count)
+    roofline = entry(f"{rs_name} (fused reduce-scatter + AdamW)", rs_bytes / len(units),
                      statistics.mean(rs_ms), "rs_adamw")
     roofline_ag = entry("all_gather_kernel (all-gather + unflatten)", ag_bytes / len(units),
                         statistics.mean(ag_ms), "all_gather")

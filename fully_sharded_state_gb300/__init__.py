@@ -11,7 +11,8 @@ from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, FSDP_ZERO3, A
                    fsdp_all_gather_unflatten, fsdp_all_gather_unflatten_units, fsdp_all_reduce,
                    fsdp_reduce_scatter_adamw_accum, fsdp_layout, fsdp_pack_flat,
                    fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_gather,
-                   fsdp_reduce_scatter_adamw_units, fsdp_version, PreparedCall,
+                   fsdp_reduce_scatter_adamw_units, fsdp_stage_wait_selftest, fsdp_stage_wait_timeouts,
+                   fsdp_version, PreparedCall,
                    prepare_fsdp_all_gather_unflatten, prepare_fsdp_all_gather_unflatten_units,
                    prepare_fsdp_reduce_scatter_adamw, prepare_fsdp_reduce_scatter_adamw_units)
 
@@ -20,7 +21,8 @@ __all__ = ["FSDP_BF16", "FSDP_F32", "FSDP_FLAT", "FSDP_PER_PARAM", "FSDP_ZERO3",
            "fsdp_all_gather_unflatten", "fsdp_all_gather_unflatten_units", "fsdp_all_reduce",
            "fsdp_reduce_scatter_adamw_accum", "fsdp_layout", "fsdp_pack_flat",
            "fsdp_reduce_scatter_adamw", "fsdp_reduce_scatter_adamw_gather",
-           "fsdp_reduce_scatter_adamw_units", "fsdp_version", "PreparedCall",
+           "fsdp_reduce_scatter_adamw_units", "fsdp_stage_wait_selftest", "fsdp_stage_wait_timeouts", "fsdp_version",
+           "PreparedCall",
            "prepare_fsdp_all_gather_unflatten", "prepare_fsdp_all_gather_unflatten_units",
            "prepare_fsdp_reduce_scatter_adamw", "prepare_fsdp_reduce_scatter_adamw_units",
            "ShardedUnit",

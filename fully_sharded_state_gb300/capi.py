@@ -108,6 +108,10 @@ def load(path: str = LIB_PATH):
     L.fsdp_write_stream.restype = ctypes.c_int
     L.fsdp_write_stream.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int64,
                                     ctypes.c_uint32, _vp]
+    L.fsdp_stage_wait_timeouts.restype = ctypes.c_int
+    L.fsdp_stage_wait_timeouts.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)]
+    L.fsdp_stage_wait_selftest.restype = ctypes.c_int
+    L.fsdp_stage_wait_selftest.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)]
     L.fsdp_last_error.restype = ctypes.c_char_p
     L.fsdp_last_error.argtypes = []
     L.fsdp_version.restype = ctypes.c_char_p
@@ -508,6 +512,31 @@ def fsdp_write_stream(dst, pattern: int = 0x3FC03FC0, stream=None) -> None:
                   else FSDP_F32)
     _check(load().fsdp_write_stream(arr, len(dst), nbytes, pattern & 0xFFFFFFFF,
                                     _stream_handle(stream)))
+
+
+def fsdp_stage_wait_timeouts(device=None) -> int:
+    """Thread blocks of the staged reduce-scatter on ``device`` (default:
+    the current CUDA device) that gave up waiting for their gradient copies
+    since the library was loaded; 0 in every valid run. Synchronises the
+    device."""
+    n = ctypes.c_uint64(0)
+    _check(load().fsdp_stage_wait_timeouts(_device_index(device), ctypes.byref(n)))
+    return int(n.value)
+
+
+def _device_index(device) -> int:
+    import torch
+    d = torch.device("cuda", device) if isinstance(device, int) else \
+        torch.device(device if device is not None else "cuda")
+    return d.index if d.index is not None else torch.cuda.current_device()
+
+
+def fsdp_stage_wait_selftest(device=None) -> int:
+    """One thread block waits on an mbarrier that nothing completes, gives up
+    after 20 ms and counts itself; returns that count (1)."""
+    n = ctypes.c_uint64(0)
+    _check(load().fsdp_stage_wait_selftest(_device_index(device), ctypes.byref(n)))
+    return int(n.value)
 
 
 def fsdp_version() -> str:

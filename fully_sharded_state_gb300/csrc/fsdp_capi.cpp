@@ -769,4 +769,18 @@ fsdp_status fsdp_write_stream(void *const *dst, int n, int64_t bytes, uint32_t p
     return launch_write_stream(dst, n, bytes, pattern, stream);
 }
 
+fsdp_status fsdp_stage_wait_timeouts(int device, uint64_t *count)
+{
+    if (count == nullptr || device < 0)
+        return set_error(FSDP_EINVAL, "fsdp_stage_wait_timeouts: bad arguments");
+    return read_stage_wait_timeouts(device, count);
+}
+
+fsdp_status fsdp_stage_wait_selftest(int device, uint64_t *gave_up)
+{
+    if (gave_up == nullptr || device < 0)
+        return set_error(FSDP_EINVAL, "fsdp_stage_wait_selftest: bad arguments");
+    return run_stage_wait_selftest(device, gave_up);
+}
+
 }  // extern "C"

@@ -84,6 +84,8 @@ fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, v
                               fsdp_dtype out_dtype, void *stream);
 fsdp_status launch_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,
                                 void *stream);
+fsdp_status read_stage_wait_timeouts(int device, uint64_t *count);
+fsdp_status run_stage_wait_selftest(int device, uint64_t *gave_up);
 fsdp_status launch_rs_adamw_gather(const fsdp_layout_t *A, const void *const *grad,
                                    float *const *master, float *const *m, float *const *v,
                                    void *const *param_shard_out, float *const *grad_shard_out,

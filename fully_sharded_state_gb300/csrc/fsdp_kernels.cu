@@ -17,7 +17,13 @@
 //
 // Segment descriptors and the per-rank pointers travel in the kernel
 // parameter block (__grid_constant__), so the kernels need no device memory
-// beyond the caller's buffers.
+// beyond the caller's buffers (and one counter of abandoned waits, below).
+//
+// The fused reduce-scatter + AdamW brings each tile's R gradient slices into
+// shared memory with cp.async.bulk, a few tiles ahead, on per-stage
+// mbarriers (rs_adamw_staged_kernel) on large launches where R is a
+// compile-time 4 or 8 (bf16 gradients) or 2 or 4 (fp32 gradients); otherwise
+// every load is a register load.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,6 +46,22 @@ constexpr int kMaxR = FSDP_MAX_RANKS;
 // Fewer CTAs, each streaming its tiles in order, keep a narrower window of
 // every buffer open at once; past these points HBM does not go faster.
 constexpr int kRsCtasPerSm = 3;
+// The staged form (gradient slices by cp.async.bulk, 3 stages of 32 KB for
+// bf16 R = 8): 1/SM 2.08 ms, 2/SM 1.327 ms on the same unit, and 1.331 ms
+// right after a gather-shaped write stream, where the register form takes
+// 1.398 ms (a replica of both kernels, one process).
+constexpr int kRsStagedCtasPerSm = 2;
+// Stage sizing: a stage (R slices of one tile) of at most kRsStageMaxBytes,
+// as many stages as fit in kRsStageBudget (2 to 8).
+constexpr int kRsStageMaxBytes = 32 * 1024;
+constexpr int kRsStageBudget = 96 * 1024;
+// When staging pays (staged / register time, flat units, alone):
+//   R x gradient bytes = 8 or 16 (bf16 R = 4, 8; fp32 R = 2, 4): 0.92-0.97
+//   from 16K tiles (54 per staged CTA), about even at 6K-8K, 1.05-1.3
+//   below 4K tiles, where the ring of stages never fills;
+//   R x gradient bytes = 4 (bf16 R = 2): 1.08-1.3 at every size.
+constexpr int kRsStageMinGradBytes = 8;
+constexpr int kRsStagedMinTilesPerCta = 32;
 // all-gather (256 threads, 16 elements per thread): 1/SM 0.613 ms,
 // 2/SM 0.668 ms, 3/SM 0.667 ms on a Llama unit, whose tiles are full and
 // aligned. A launch whose elements mostly sit in misaligned or partial tiles
@@ -159,6 +181,100 @@ __device__ __forceinline__ float4 ld_f4(const float *p)
 __device__ __forceinline__ void st_f4(float *p, float4 v)
 {
     __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+// ---------------------------------------- bulk copies and mbarriers ----
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One arrival that also announces `bytes` of bulk copies to come.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for phase `parity` of `bar` for at most `limit_ns` of the global
+// timer, and at most 2^27 polls should the timer not advance; false if it
+// gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t round = 0; round < (1u << 22); round++) {
+        for (int k = 0; k < 32; k++)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+constexpr uint64_t kStageWaitNs = 2000000000ull;  // a stage's copies: 2 s
+
+// CTAs that gave up waiting for their bulk copies (read by the host through
+// fsdp_stage_wait_timeouts). Zero unless a copy failed to arrive.
+__device__ unsigned long long g_stage_wait_timeouts;
+// The same count for the self-test below, kept apart so that it never
+// touches the real one.
+__device__ unsigned long long g_selftest_wait_timeouts;
+
+// Self-test of the bounded wait: one CTA waits on an mbarrier whose phase
+// cannot complete (one arrival announcing 16 bytes that no copy delivers),
+// gives up after limit_ns and counts itself. No copy is in flight, so the
+// CTA may leave with the phase open.
+__global__ void stage_wait_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        mbar_arrive_expect_tx(&bar, 16);
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0)
+        atomicAdd(&g_selftest_wait_timeouts, 1ull);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -639,6 +755,45 @@ __device__ __forceinline__ void fold8_accum(const RankPtrs &b, int R, int64_t j,
     }
 }
 
+// The 8 shard elements at s of one rank: acc holds their rank-ordered
+// gradient sums (scaled by 1/R here), w/m/v their loaded state. AdamW, then
+// the stores of master, m, v, the bf16 shard and the gradient shard.
+template <bool kParamBf16>
+__device__ __forceinline__ void adamw8_store(const AdamScalars &c, const RankPtrs &b, int64_t s,
+                                             float acc[8], float4 w0, float4 w1, float4 m0,
+                                             float4 m1, float4 v0, float4 v1)
+{
+    float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        acc[k] = __fmul_rn(acc[k], c.inv_R);
+        AdamOut o = adamw_elem(c, acc[k], wv[k], mv[k], vv[k]);
+        wv[k] = o.w;
+        mv[k] = o.m;
+        vv[k] = o.v;
+    }
+    st_f4(b.master + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
+    st_f4(b.master + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
+    st_f4(b.m + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
+    st_f4(b.m + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
+    st_f4(b.v + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    st_f4(b.v + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    if (kParamBf16) {
+        uint4 o;
+        o.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
+        o.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
+        o.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
+        st_stream(b.pshard + s, o);
+    }
+    if (b.gshard) {
+        st_f4(b.gshard + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_f4(b.gshard + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+}
+
 // One reduce-scatter + AdamW tile.
 template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
@@ -695,35 +850,7 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
         fold8_accum<RC, kGradBf16>(b, R, j, acc);
     else
         fold8<RC, kGradBf16>(b.grad, R, j, acc);
-    float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        acc[k] = __fmul_rn(acc[k], p.c.inv_R);
-        AdamOut o = adamw_elem(p.c, acc[k], wv[k], mv[k], vv[k]);
-        wv[k] = o.w;
-        mv[k] = o.m;
-        vv[k] = o.v;
-    }
-    st_f4(b.master + s, make_float4(wv[0], wv[1], wv[2], wv[3]));
-    st_f4(b.master + s + 4, make_float4(wv[4], wv[5], wv[6], wv[7]));
-    st_f4(b.m + s, make_float4(mv[0], mv[1], mv[2], mv[3]));
-    st_f4(b.m + s + 4, make_float4(mv[4], mv[5], mv[6], mv[7]));
-    st_f4(b.v + s, make_float4(vv[0], vv[1], vv[2], vv[3]));
-    st_f4(b.v + s + 4, make_float4(vv[4], vv[5], vv[6], vv[7]));
-    if (kParamBf16) {
-        uint4 o;
-        o.x = (uint32_t)f32_to_bf16_bits(wv[0]) | ((uint32_t)f32_to_bf16_bits(wv[1]) << 16);
-        o.y = (uint32_t)f32_to_bf16_bits(wv[2]) | ((uint32_t)f32_to_bf16_bits(wv[3]) << 16);
-        o.z = (uint32_t)f32_to_bf16_bits(wv[4]) | ((uint32_t)f32_to_bf16_bits(wv[5]) << 16);
-        o.w = (uint32_t)f32_to_bf16_bits(wv[6]) | ((uint32_t)f32_to_bf16_bits(wv[7]) << 16);
-        st_stream(b.pshard + s, o);
-    }
-    if (b.gshard) {
-        st_f4(b.gshard + s, make_float4(acc[0], acc[1], acc[2], acc[3]));
-        st_f4(b.gshard + s + 4, make_float4(acc[4], acc[5], acc[6], acc[7]));
-    }
+    adamw8_store<kParamBf16>(p.c, b, s, acc, w0, w1, m0, m1, v0, v1);
 }
 
 // kUnits as for the all-gather.
@@ -736,6 +863,192 @@ __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constan
         if (!kUnits)
             T.base = 0;
         rs_adamw_tile<RC, kGradBf16, kParamBf16, kAccum>(p, R, T);
+    }
+}
+
+// ------------------------------ reduce-scatter + AdamW, staged gradients ----
+//
+// The same tiles and arithmetic as rs_adamw_kernel, with each tile's R
+// gradient slices brought into shared memory by cp.async.bulk: thread 0
+// issues R 1-D copies of the tile onto its stage's mbarrier, stages() tiles
+// ahead of the threads that consume them, and re-fills a stage once every
+// thread has read it. The threads load the fp32 state (master, m, v) of
+// their 8 elements themselves, before they wait. A tile whose start is
+// misaligned in the full or the shard buffer, and the last partial vector of
+// a tile, take rs_adamw_tile (their stage carries no bytes).
+//
+// Every wait gives up after kStageWaitNs: the CTA then counts itself in
+// g_stage_wait_timeouts, lets the copies it issued land (again bounded) and
+// returns, leaving its remaining tiles unwritten.
+
+constexpr int stages_for(int stage_bytes)
+{
+    return stage_bytes <= 0 ? 1
+           : kRsStageBudget / stage_bytes < 2 ? 2
+           : kRsStageBudget / stage_bytes > 8 ? 8
+                                              : kRsStageBudget / stage_bytes;
+}
+
+template <int RC, bool kGradBf16>
+struct RsStage {
+    static constexpr int kEB = kGradBf16 ? 2 : 4;
+    static constexpr int kSlice = (int)kTile * kEB;  // one rank's slice of a tile
+    static constexpr int kBytes = RC * kSlice;       // one stage
+    static constexpr bool kOn =
+        RC > 0 && RC * kEB >= kRsStageMinGradBytes && kBytes <= kRsStageMaxBytes;
+    static constexpr int stages() { return stages_for(kBytes); }
+    static constexpr size_t smem();
+};
+
+template <bool kUnits, class PP>
+__device__ __forceinline__ Tile rs_tile(const PP &p, int64_t t)
+{
+    Tile T = locate<kTile>(p.seg, p.nseg, t, false);
+    if (!kUnits)
+        T.base = 0;
+    return T;
+}
+
+__device__ __forceinline__ bool vector_aligned(const Tile &T)
+{
+    return ((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0;
+}
+
+// The rank-ordered fold of the 8 staged gradient elements at tile offset e.
+template <int RC, bool kGradBf16>
+__device__ __forceinline__ void fold8_staged(const unsigned char *st, int64_t e, float acc[8])
+{
+    using S = RsStage<RC, kGradBf16>;
+    if (kGradBf16) {
+        uint4 raw[RC];
+#pragma unroll
+        for (int q = 0; q < RC; q++)
+            raw[q] = *reinterpret_cast<const uint4 *>(st + q * S::kSlice + e * 2);
+        unpack_bf16x8(raw[0], acc);
+#pragma unroll
+        for (int q = 1; q < RC; q++) {
+            float g[8];
+            unpack_bf16x8(raw[q], g);
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                acc[k] = __fadd_rn(acc[k], g[k]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < RC; q++) {
+            const float4 a = *reinterpret_cast<const float4 *>(st + q * S::kSlice + e * 4);
+            const float4 c = *reinterpret_cast<const float4 *>(st + q * S::kSlice + e * 4 + 16);
+            const float g[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                acc[k] = q == 0 ? g[k] : __fadd_rn(acc[k], g[k]);
+        }
+    }
+}
+
+// What the consumers of a stage need of its tile, written by thread 0 when
+// it issues the tile's copies: the consumers read it from shared memory
+// instead of searching the segment table and indexing the parameter block.
+struct StageTile {
+    Tile T;
+    RankPtrs b;
+};
+
+template <int RC, bool kGradBf16>
+constexpr size_t RsStage<RC, kGradBf16>::smem()
+{
+    return (size_t)stages() * (kBytes + sizeof(uint64_t) + sizeof(StageTile));
+}
+
+template <int RC, bool kGradBf16, bool kParamBf16, bool kUnits>
+__global__ void __launch_bounds__(kThreads, kRsStagedCtasPerSm)
+    rs_adamw_staged_kernel(const __grid_constant__ RsParams p)
+{
+    using S = RsStage<RC, kGradBf16>;
+    static_assert(S::kOn, "staging needs a compile-time R whose stage fits");
+    constexpr int NS = S::stages();
+    extern __shared__ __align__(128) unsigned char stage[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(stage + (size_t)NS * S::kBytes);
+    StageTile *desc = reinterpret_cast<StageTile *>(bar + NS);
+    const int tid = threadIdx.x;
+    // thread 0: tile t's descriptor and gradient copies onto stage k (no
+    // copies for a misaligned tile: its phase completes at once)
+    auto issue = [&](const Tile &T, int k) {
+        desc[k].T = T;
+        desc[k].b = rank_ptrs(p, T);
+        const uint32_t bytes =
+            vector_aligned(T) ? (uint32_t)((T.len * S::kEB) & ~(int64_t)15) : 0u;
+        mbar_arrive_expect_tx(&bar[k], bytes * RC);
+        if (bytes != 0) {
+            unsigned char *dst = stage + (size_t)k * S::kBytes;
+#pragma unroll
+            for (int q = 0; q < RC; q++)
+                bulk_load(dst + q * S::kSlice,
+                          static_cast<const unsigned char *>(p.grad[T.base + q]) +
+                              T.fbase * S::kEB,
+                          bytes, &bar[k]);
+        }
+    };
+    if (tid == 0) {
+        for (int k = 0; k < NS; k++)
+            mbar_init(&bar[k], 1);
+        mbar_init_fence();
+        for (int k = 0; k < NS; k++) {
+            const int64_t t = blockIdx.x + (int64_t)k * gridDim.x;
+            if (t < p.total_tiles)
+                issue(rs_tile<kUnits>(p, t), k);
+        }
+    }
+    __syncthreads();
+    const int64_t e = (int64_t)tid * kElemsPerThread;
+    int64_t i = 0;  // this CTA's tile count: stage i % NS, phase i / NS
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, i++) {
+        const int k = (int)(i % NS);
+        // written by thread 0 at least one barrier ago
+        const Tile T = desc[k].T;
+        const RankPtrs b = desc[k].b;
+        const bool vec = vector_aligned(T) && e + kElemsPerThread <= T.len;
+        const int64_t s = T.sbase + e;
+        float4 w0, w1, m0, m1, v0, v1;
+        if (vec) {
+            w0 = ld_f4(b.master + s);
+            w1 = ld_f4(b.master + s + 4);
+            m0 = ld_f4(b.m + s);
+            m1 = ld_f4(b.m + s + 4);
+            v0 = ld_f4(b.v + s);
+            v1 = ld_f4(b.v + s + 4);
+        }
+        // thread 0 finds the tile that will refill stage k while its loads fly
+        const int64_t tn = t + (int64_t)NS * gridDim.x;
+        Tile Tn;
+        if (tid == 0 && tn < p.total_tiles)
+            Tn = rs_tile<kUnits>(p, tn);
+        const bool ok = mbar_wait_bounded(&bar[k], (uint32_t)((i / NS) & 1), kStageWaitNs);
+        if (ok) {
+            if (vec) {
+                float acc[8];
+                fold8_staged<RC, kGradBf16>(stage + (size_t)k * S::kBytes, e, acc);
+                adamw8_store<kParamBf16>(p.c, b, s, acc, w0, w1, m0, m1, v0, v1);
+            } else {
+                rs_adamw_tile<RC, kGradBf16, kParamBf16, false>(p, RC, T);
+            }
+        }
+        // every thread is done with stage k; all learn whether a wait gave up
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicAdd(&g_stage_wait_timeouts, 1ull);
+                // the copies of this tile and the next NS - 1 were issued
+                for (int j = 0; j < NS; j++) {
+                    if (t + (int64_t)j * gridDim.x >= p.total_tiles)
+                        break;
+                    const int64_t ij = i + j;
+                    mbar_wait_bounded(&bar[ij % NS], (uint32_t)((ij / NS) & 1), kStageWaitNs);
+                }
+            }
+            return;
+        }
+        if (tid == 0 && tn < p.total_tiles)
+            issue(Tn, k);
     }
 }
 
@@ -1026,7 +1339,7 @@ class DeviceScope {
 // Persistent grid size for `kernel` on `dev`: resident CTAs per SM (at most
 // `max_per_sm`) x SMs.
 fsdp_status grid_for(int dev, const void *kernel, int threads, int64_t tiles, int max_per_sm,
-                     int *grid)
+                     int *grid, size_t smem = 0)
 {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo &d = g_dev[dev];
@@ -1036,8 +1349,12 @@ fsdp_status grid_for(int dev, const void *kernel, int threads, int64_t tiles, in
         return set_error(FSDP_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(err));
     auto it = d.blocks_per_sm.find(kernel);
     if (it == d.blocks_per_sm.end()) {
+        if (smem > 48 * 1024 &&
+            (err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem)) != cudaSuccess)
+            return set_error(FSDP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(err));
         int nb = 0;
-        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0)) !=
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem)) !=
             cudaSuccess)
             return set_error(FSDP_ECUDA, "cudaOccupancyMaxActiveBlocksPerMultiprocessor: %s",
                              cudaGetErrorString(err));
@@ -1067,14 +1384,14 @@ void fill_segs(Params &p, const LaunchPlan &plan)
 
 template <typename Params, typename Kernel>
 fsdp_status run(int dev, Kernel kernel, Params &p, cudaStream_t stream, const char *what,
-                int max_per_sm, int threads = kThreads)
+                int max_per_sm, int threads = kThreads, size_t smem = 0)
 {
     int grid = 0;
     fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), threads,
-                              p.total_tiles, max_per_sm, &grid);
+                              p.total_tiles, max_per_sm, &grid, smem);
     if (st != FSDP_OK)
         return st;
-    kernel<<<grid, threads, 0, stream>>>(p);
+    kernel<<<grid, threads, smem, stream>>>(p);
     return check_launch(what);
 }
 
@@ -1240,16 +1557,37 @@ fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void 
     return FSDP_OK;
 }
 
+// The staged kernel where R is a compile-time constant whose stage fits, no
+// accumulators are read and the launch gives every staged CTA at least
+// kRsStagedMinTilesPerCta tiles; the register kernel otherwise.
+template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
+static fsdp_status rs_run(int dev, RsParams &p, cudaStream_t s)
+{
+    using S = RsStage<RC, kGradBf16>;
+    if constexpr (!kAccum && S::kOn) {
+        auto kernel = rs_adamw_staged_kernel<RC, kGradBf16, kParamBf16, kUnits>;
+        int grid = 0;
+        fsdp_status st = grid_for(dev, reinterpret_cast<const void *>(kernel), kThreads,
+                                  p.total_tiles, kRsStagedCtasPerSm, &grid, S::smem());
+        if (st != FSDP_OK)
+            return st;
+        if (p.total_tiles >= (int64_t)kRsStagedMinTilesPerCta * grid) {
+            kernel<<<grid, kThreads, S::smem(), s>>>(p);
+            return check_launch("rs_adamw_staged");
+        }
+    }
+    return run(dev, rs_adamw_kernel<RC, kGradBf16, kParamBf16, kAccum, kUnits>, p, s,
+               "rs_adamw", kRsCtasPerSm);
+}
+
 template <bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
 static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
 {
-    const char *w = "rs_adamw";
-    const int per = kRsCtasPerSm;
     switch (R) {
-    case 2: return run(dev, rs_adamw_kernel<2, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
-    case 4: return run(dev, rs_adamw_kernel<4, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
-    case 8: return run(dev, rs_adamw_kernel<8, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
-    default: return run(dev, rs_adamw_kernel<0, kGradBf16, kParamBf16, kAccum, kUnits>, p, s, w, per);
+    case 2: return rs_run<2, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
+    case 4: return rs_run<4, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
+    case 8: return rs_run<8, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
+    default: return rs_run<0, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
     }
 }
 
@@ -1411,6 +1749,52 @@ fsdp_status launch_write_stream(void *const *dst, int n, int64_t bytes, uint32_t
         return st;
     write_stream_kernel<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(p);
     return check_launch("write_stream");
+}
+
+fsdp_status run_stage_wait_selftest(int device, uint64_t *gave_up)
+{
+    int prev = -1;
+    cudaError_t err = cudaGetDevice(&prev);
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+    if (prev != device && (err = cudaSetDevice(device)) != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaSetDevice(%d): %s", device, cudaGetErrorString(err));
+    unsigned long long before = 0, after = 0;
+    err = cudaMemcpyFromSymbol(&before, g_selftest_wait_timeouts, sizeof before);
+    if (err == cudaSuccess) {
+        stage_wait_selftest_kernel<<<1, 32>>>(20000000ull);  // gives up after 20 ms
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess)
+        err = cudaDeviceSynchronize();
+    if (err == cudaSuccess)
+        err = cudaMemcpyFromSymbol(&after, g_selftest_wait_timeouts, sizeof after);
+    if (prev != device)
+        cudaSetDevice(prev);
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "wait self-test: %s", cudaGetErrorString(err));
+    *gave_up = after - before;
+    return FSDP_OK;
+}
+
+fsdp_status read_stage_wait_timeouts(int device, uint64_t *count)
+{
+    int prev = -1;
+    cudaError_t err = cudaGetDevice(&prev);
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+    if (prev != device && (err = cudaSetDevice(device)) != cudaSuccess)
+        return set_error(FSDP_ECUDA, "cudaSetDevice(%d): %s", device, cudaGetErrorString(err));
+    unsigned long long n = 0;
+    err = cudaDeviceSynchronize();
+    if (err == cudaSuccess)
+        err = cudaMemcpyFromSymbol(&n, g_stage_wait_timeouts, sizeof n);
+    if (prev != device)
+        cudaSetDevice(prev);
+    if (err != cudaSuccess)
+        return set_error(FSDP_ECUDA, "reading the wait-timeout count: %s", cudaGetErrorString(err));
+    *count = n;
+    return FSDP_OK;
 }
 
 }  // namespace fsdp

@@ -176,7 +176,12 @@ typedef struct {
  * master/m/v[r]: fp32 shard buffers, read and written. param_shard_out[r]:
  * BF16 layouts only (else NULL): receives bf16 RNE of the new master.
  * grad_shard_out: NULL, or R fp32 shard buffers that receive g (for checks;
- * not needed for training). step >= 1; 0 <= beta1, beta2 < 1; eps > 0. */
+ * not needed for training). step >= 1; 0 <= beta1, beta2 < 1; eps > 0.
+ * For R = 4 or 8 (bf16 gradients) and R = 2 or 4 (fp32 gradients), on
+ * launches of at least ~10,000 tiles of 2,048 elements (units of ~20M
+ * parameters and up), the kernel stages the gradient slices in shared memory
+ * with bulk copies and waits for them at most ~2 s; see
+ * fsdp_stage_wait_timeouts. The results are the same either way. */
 fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *layout, const void *const *grad_full,
                                       float *const *master, float *const *m, float *const *v,
                                       void *const *param_shard_out, float *const *grad_shard_out,
@@ -283,6 +288,26 @@ fsdp_status fsdp_reduce_scatter_adamw_units(int n_units, const fsdp_layout_t *co
  * all-reduce. Errors: FSDP_EINVAL, FSDP_EALIGN, FSDP_ECUDA. */
 fsdp_status fsdp_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,
                               void *stream);
+
+/* Implementation status; the pages have no counterpart. The number of
+ * thread blocks of the staged reduce-scatter kernel on CUDA device `device`
+ * that gave up waiting for their gradient bulk copies (after ~2 s each),
+ * since the library was loaded. A block that gives up leaves the rest of its
+ * tiles unwritten, so any nonzero count means the results of the calls
+ * since the last read of 0 are invalid. Waits for all work on the device
+ * (cudaDeviceSynchronize) before it reads; restores the caller's current
+ * device. Errors: FSDP_EINVAL (count NULL, device < 0), FSDP_ECUDA. */
+fsdp_status fsdp_stage_wait_timeouts(int device, uint64_t *count);
+
+/* Self-test of that bounded wait; the pages have no counterpart. Launches
+ * one thread block on `device` that waits on an mbarrier whose phase cannot
+ * complete (bytes announced that no copy delivers), gives up after 20 ms and
+ * counts itself in a counter of its own (fsdp_stage_wait_timeouts is not
+ * touched). *gave_up receives the number of blocks that gave up: 1. The
+ * device stays usable. Synchronises the device; restores the caller's
+ * current device. Errors: FSDP_EINVAL (gave_up NULL, device < 0),
+ * FSDP_ECUDA. */
+fsdp_status fsdp_stage_wait_selftest(int device, uint64_t *gave_up);
 
 /* Message for the last non-OK status returned on the calling thread. */
 const char *fsdp_last_error(void);

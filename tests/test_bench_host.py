@@ -40,6 +40,26 @@ def _rank_main(rank, world, port, out):
     dist.destroy_process_group()
 
 
+def test_rs_kernel_name_follows_the_staging_rule():
+    from fully_sharded_state_gb300 import synth
+    llama = synth.WORKLOADS["llama4"].unit_shapes(0)
+    block = synth.WORKLOADS["block"].unit_shapes(0)
+    # Llama unit: 106K tiles at R = 8, bf16 gradients
+    assert bench.rs_kernel_name(llama, 8, 2, 152) == "rs_adamw_staged_kernel"
+    assert bench.rs_kernel_name(llama, 4, 2, 152) == "rs_adamw_staged_kernel"
+    assert bench.rs_kernel_name(llama, 2, 4, 152) == "rs_adamw_staged_kernel"
+    # too few gradient bytes per element, or a stage over 32 KB, or R unknown
+    # at compile time
+    assert bench.rs_kernel_name(llama, 2, 2, 152) == "rs_adamw_kernel"
+    assert bench.rs_kernel_name(llama, 8, 4, 152) == "rs_adamw_kernel"
+    assert bench.rs_kernel_name(llama, 16, 2, 152) == "rs_adamw_kernel"
+    # the 3.1M-parameter block: 1,536 tiles, under 32 per staged thread block
+    assert bench.rs_kernel_name(block, 4, 2, 152) == "rs_adamw_kernel"
+    # the bar: 32 tiles x 2 thread blocks x SMs
+    assert bench.rs_kernel_name([(9728 * 2048,)], 4, 2, 152) == "rs_adamw_staged_kernel"
+    assert bench.rs_kernel_name([(9724 * 2048,)], 4, 2, 152) == "rs_adamw_kernel"
+
+
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
     out = mp.Manager().dict()
