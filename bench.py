@@ -854,7 +854,21 @@ def run_e2e(args, units, grads, h_grads, full, hp, stream, dev, world, step_byte
                     h_out[k][r].copy_(U.param_shard[r], non_blocking=True)
             d2h_done[k].record(d2h_stream)
 
+    def link_gbs():
+        # the host link over the same buffers, with no kernels: every unit's
+        # gradients copied once on the two copy streams
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        for k in range(len(units)):
+            for c, hs in enumerate(h2d_streams):
+                with torch.cuda.stream(hs):
+                    for r in range(c, R, len(h2d_streams)):
+                        grads[k][r].copy_(h_grads[k][r], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        return round(h2d / (time.perf_counter() - t) / 1e9, 1)
+
     e2e_step()
+    link_before = link_gbs()
     torch.cuda.synchronize(dev)
     barrier(world)
     t0 = time.perf_counter()
@@ -863,10 +877,12 @@ def run_e2e(args, units, grads, h_grads, full, hp, stream, dev, world, step_byte
     torch.cuda.synchronize(dev)
     barrier(world)
     dt = max_over_ranks(time.perf_counter() - t0, world)
+    link_after = link_gbs()
     return {"value": round(world * step_bytes * steps / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1e3 * dt / steps, 3),
             "h2d_GBps": round(h2d * steps / dt / 1e9, 1),
+            "h2d_link_GBps_before_after": [link_before, link_after],
             "path": "each unit's own pinned host grads -> device on two copy streams running "
                     "ahead, per-unit all-gather + reduce-scatter/AdamW on the compute stream, "
                     "bf16 shards -> pinned host on a fourth stream; host wall clock"}

@@ -26,6 +26,9 @@ def test_bench_line_contract(cuda_lib, capsys):
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    # the host link's own rate over the same buffers, just before and after
+    assert len(e2e["h2d_link_GBps_before_after"]) == 2
+    assert all(x > 0 for x in e2e["h2d_link_GBps_before_after"])
     assert "workload" in line["config"]
     for entry in (line["roofline_all_gather"], line["ddp_all_reduce"], line["pack"],
                   *line["grad_accumulation"].values()):
