@@ -108,18 +108,22 @@ def test_llama_unit_full_size_sampled(cuda_lib, u):
     torch.cuda.synchronize()
 
 
-def test_unit_past_two_to_the_31_elements(cuda_lib):
-    """A FlatParameter unit of 2^31 + 4,097 bf16 elements over R = 2 (about
-    47 GB on the device): element offsets and tile indices pass 2^31, so the
-    64-bit index paths run. Samples cluster around 2^31, the rank boundary
-    and the end of the unit."""
+@pytest.mark.parametrize("R,P", [
+    (2, (1 << 31) + 4097),   # the register reduce-scatter (bf16, R = 2)
+    (4, (1 << 31) + 32768),  # the staged one; rank 3's aligned piece straddles 2^31
+])
+def test_unit_past_two_to_the_31_elements(cuda_lib, R, P):
+    """A FlatParameter unit of just over 2^31 bf16 elements (about 47-64 GB
+    on the device): element offsets and tile indices pass 2^31, and byte
+    offsets pass 4 GB, so the 64-bit index paths run, including the staged
+    reduce-scatter's bulk-copy addresses at R = 4. Samples cluster around
+    2^31, the rank boundaries and the end of the unit."""
     dev = torch.device("cuda")
-    P = (1 << 31) + 4097
     shapes = [(P,)]
-    U = ShardedUnit(shapes, 2, "flat", "bf16", "bf16")
-    O = oracle.layout(oracle.FLAT, 2, shapes)
+    U = ShardedUnit(shapes, R, "flat", "bf16", "bf16")
+    O = oracle.layout(oracle.FLAT, R, shapes)
     assert (U.P, U.S) == (O.full_numel, O.shard_numel)
-    for r in range(2):
+    for r in range(R):
         U.param_shard[r].copy_(synth.device_normal(900 + r, U.S, 0.02, dev, torch.bfloat16))
         U.master[r].copy_(synth.device_normal(910 + r, U.S, 0.02, dev))
         U.m[r].copy_(synth.device_normal(920 + r, U.S, 1e-4, dev))
@@ -128,7 +132,7 @@ def test_unit_past_two_to_the_31_elements(cuda_lib):
         del z
     rng = np.random.default_rng(7)
     js = set()
-    for c in (0, U.S - 1, U.S, 1 << 31, P - 1):
+    for c in [0, 1 << 31, P - 1] + [r * U.S + o for r in range(1, R) for o in (-1, 0)]:
         js.update(range(max(0, c - 40), min(P, c + 40)))
     js.update(rng.integers(0, P, 20000).tolist())
     js = np.array(sorted(js), np.int64)
@@ -138,13 +142,13 @@ def test_unit_past_two_to_the_31_elements(cuda_lib):
     full = U.alloc_full()
     U.all_gather(full)
     want = _at(U.param_shard, rank, idx, dev)
-    for d in range(2):
+    for d in range(R):
         assert_bits_equal(host(full[d][jt]), want, f"full[{d}] past 2^31")
     del full
-    grads = [synth.device_normal(940 + q, P, 1e-3, dev, torch.bfloat16) for q in range(2)]
+    grads = [synth.device_normal(940 + q, P, 1e-3, dev, torch.bfloat16) for q in range(R)]
     hp = AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
     ohp = oracle.AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
-    g_s = [host(grads[q][jt]) for q in range(2)]
+    g_s = [host(grads[q][jt]) for q in range(R)]
     w_s, m_s, v_s = (_at(b, rank, idx, dev) for b in (U.master, U.m, U.v))
     U.reduce_scatter_adamw(grads, hp, step=2)
     torch.cuda.synchronize()
