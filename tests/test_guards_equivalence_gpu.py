@@ -2,8 +2,9 @@
 
 Guards: every output buffer sits inside a larger allocation whose bytes
 before and after it hold a known pattern; after pack, gather, reduce-scatter
-+ AdamW (with and without accumulators), all-reduce and accumulation the
-patterns must be intact, so no kernel writes outside its buffers.
++ AdamW (with and without accumulators, register and staged kernels),
+all-reduce and accumulation the patterns must be intact, so no kernel writes
+outside its buffers.
 
 Equivalence ("FSDP2 的参数全聚合、梯度归约分片与显存峰值", §12): one sharded
 step equals one step of torch.optim.AdamW on the full parameters with the
@@ -44,6 +45,11 @@ class Guarded:
     ("flat", "bf16", "f32", 3, [(1001, 3), (5, 7)]),
     ("zero3", "f32", "bf16", 8, [(127, 513), (3, 1), (4097, 1), (9,)]),
     ("per_param", "f32", "f32", 9, [(2049, 1), (33, 8)]),
+    # 24.6M parameters: large enough for the reduce-scatter that stages its
+    # gradient slices in shared memory; rows of 4,097 put most rank pieces
+    # off the 8-element grid, so staged and register tiles share the launch
+    ("per_param", "bf16", "bf16", 8, [(6000, 4097), (7, 513), (64,)]),
+    ("per_param", "bf16", "f32", 4, [(6000, 4097), (5, 3)]),
 ])
 def test_kernels_write_only_inside_their_buffers(cuda_lib, mode, pdt, gdt, R, shapes):
     G = Guarded()
