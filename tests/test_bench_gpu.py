@@ -72,3 +72,39 @@ def test_peak_memory_matches_the_pages_formula(cuda_lib):
         want = formulas.peak_bytes(m_shard, full_unit, prefetch, activations=0, temp=full_unit)
         assert want == Fraction(got[sched]["formula_bytes"])
         assert abs(got[sched]["measured_bytes"] - want) <= 65536, (sched, got[sched])
+
+
+@pytest.mark.parametrize("shapes,R,gdt", [
+    ([(4096, 4096), (1024, 4096), (4096,)], 8, "bf16"),  # staged
+    ([(6000, 4097)], 4, "f32"),                           # staged, fp32 gradients
+    ([(512, 512), (512,)], 4, "bf16"),                    # too few tiles: register
+    ([(6000, 4097)], 2, "bf16"),                          # 4 gradient bytes: register
+    ([(6000, 4097)], 8, "f32"),                           # a 64 KB stage: register
+])
+def test_rs_kernel_name_matches_the_launched_kernel(cuda_lib, shapes, R, gdt):
+    """The kernel bench.py names in its roofline is the one the library
+    launches: the reduce-scatter runs under torch.profiler (CUPTI sees every
+    kernel in the process) and the recorded name must match."""
+    import torch
+    from torch.profiler import ProfilerActivity, profile
+
+    from fully_sharded_state_gb300 import AdamWHP, ShardedUnit
+
+    U = ShardedUnit(shapes, R, "per_param", "bf16", gdt)
+    U.shard_from_full(torch.randn(U.P, device="cuda") * 0.02)
+    grads = U.alloc_grads()
+    for g in grads:
+        g.normal_(0, 1e-3)
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]):  # the first session starts CUPTI
+        torch.zeros(1, device="cuda").add_(1)
+        torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        U.reduce_scatter_adamw(grads, AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01))
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if "rs_adamw" in e.name]
+    assert names, "the profiler recorded no reduce-scatter kernel"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want = bench.rs_kernel_name(U.shapes, R, 2 if gdt == "bf16" else 4, sms)
+    assert any(want + "<" in n for n in names), (want, names)
+
