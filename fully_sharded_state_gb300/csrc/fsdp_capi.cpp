@@ -401,7 +401,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
         L->shard_rows.push_back(rows);
         L->shard_off.push_back(seg_total);
         if (mode == FSDP_PER_PARAM)
-            segs.push_back({P, numel, stride, seg_total, pad, 0, 0, -1, 0});
+            segs.push_back({P, numel, stride, seg_total, pad, 0, 0, -1, 0, 0});
         P += numel;
         seg_total += pad;
     }
@@ -411,7 +411,7 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
     } else if (mode == FSDP_FLAT) {
         int64_t S = ceil_div(P, R);
         L->shard_numel = S;
-        segs.push_back({0, P, S, 0, S, 0, 0, -1, 0});
+        segs.push_back({0, P, S, 0, S, 0, 0, -1, 0, 0});
     } else {
         std::vector<int64_t> numel(n_params);
         for (int i = 0; i < n_params; i++)
@@ -424,12 +424,14 @@ fsdp_status fsdp_layout(fsdp_mode mode, int R, int n_params, const int64_t *dim0
             const int64_t pad = ceil_div(numel[i], FSDP_SEG_ALIGN) * FSDP_SEG_ALIGN;
             L->shard_rows[i] = dim0[i];
             L->shard_off[i] = used[o];
-            segs.push_back({L->full_off[i], numel[i], numel[i], used[o], pad, 0, 0, (int32_t)o, 0});
+            segs.push_back({L->full_off[i], numel[i], numel[i], used[o], pad, 0, 0, (int32_t)o, 0, 0});
             used[o] += pad;
             longest = std::max(longest, used[o]);
         }
         L->shard_numel = longest;
     }
+    for (Seg &sg : segs)
+        sg.unit_numel = P;
     int64_t padded;
     if (!mul_ok(L->shard_numel, R, &padded)) {
         delete L;

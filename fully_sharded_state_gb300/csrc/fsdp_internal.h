@@ -39,6 +39,8 @@ struct Seg {
                              // (numel elements) belongs to this rank
     int32_t base;            // where this segment's unit starts in the launch's per-rank
                              // pointer arrays: rank r's buffer is entry base + r
+    int64_t unit_numel;      // P of the segment's unit: the length of its full and
+                             // gradient buffers
 };
 
 // The segments of one launch and its tile count. elems: the elements its

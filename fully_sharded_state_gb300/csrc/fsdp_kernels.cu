@@ -51,10 +51,14 @@ constexpr int kRsCtasPerSm = 3;
 // right after a gather-shaped write stream, where the register form takes
 // 1.398 ms (a replica of both kernels, one process).
 constexpr int kRsStagedCtasPerSm = 2;
-// Stage sizing: a stage (R slices of one tile) of at most kRsStageMaxBytes,
-// as many stages as fit in kRsStageBudget (2 to 8).
+// Stage sizing: a stage (R slices of one tile) of at most kRsStageMaxBytes
+// of gradients, and as many stages (2 to 8) as fit, with their barriers and
+// tile descriptors, in kRsStagedSmemBudget: two CTAs and their 1 KB
+// reservations then fit the 196 KB shared-memory carveout. Past it the SM
+// takes the 228 KB carveout, L1 drops from 60 KB to 28 KB, and a Llama unit's
+// reduce-scatter took 1.351 ms instead of 1.305.
 constexpr int kRsStageMaxBytes = 32 * 1024;
-constexpr int kRsStageBudget = 96 * 1024;
+constexpr int kRsStagedSmemBudget = 97 * 1024;
 // When staging pays (staged / register time, flat units, alone):
 //   R x gradient bytes = 8 or 16 (bf16 R = 4, 8; fp32 R = 2, 4): 0.92-0.97
 //   from 16K tiles (54 per staged CTA), about even at 6K-8K, 1.05-1.3
@@ -122,6 +126,7 @@ struct Tile {
     int64_t sbase;   // shard-buffer index of the tile's first element
     int64_t len;     // elements in the tile
     int64_t nvalid;  // padded traversal: elements of the tile that the rank owns
+    int64_t unit_numel;  // P of the tile's unit (the full and gradient buffers' length)
 };
 
 // kT: the kernel's tile length.
@@ -161,6 +166,7 @@ __device__ __forceinline__ Tile locate(const Seg *seg, int nseg, int64_t t, bool
     T.len = piece - off < kT ? piece - off : kT;
     int64_t nv = owned - off;
     T.nvalid = nv < 0 ? 0 : (nv > T.len ? T.len : nv);
+    T.unit_numel = s.unit_numel;
     return T;
 }
 
@@ -873,32 +879,85 @@ __global__ void __launch_bounds__(kThreads) rs_adamw_kernel(const __grid_constan
 // issues R 1-D copies of the tile onto its stage's mbarrier, stages() tiles
 // ahead of the threads that consume them, and re-fills a stage once every
 // thread has read it. The threads load the fp32 state (master, m, v) of
-// their 8 elements themselves, before they wait. A tile whose start is
-// misaligned in the full or the shard buffer, and the last partial vector of
-// a tile, take rs_adamw_tile (their stage carries no bytes).
+// their 8 elements themselves, before they wait. A tile whose start is off a
+// 16-byte boundary in the full buffer is staged from the boundary below it
+// and realigned in registers (fold8_staged_at); shard offsets are always
+// multiples of 8. The last partial vector of a tile goes element by element.
 //
 // Every wait gives up after kStageWaitNs: the CTA then counts itself in
 // g_stage_wait_timeouts, lets the copies it issued land (again bounded) and
 // returns, leaving its remaining tiles unwritten.
 
-constexpr int stages_for(int stage_bytes)
+// per_stage: a stage's slices, barrier and tile descriptor, in bytes
+constexpr int stages_for(int per_stage)
 {
-    return stage_bytes <= 0 ? 1
-           : kRsStageBudget / stage_bytes < 2 ? 2
-           : kRsStageBudget / stage_bytes > 8 ? 8
-                                              : kRsStageBudget / stage_bytes;
+    return per_stage <= 0 ? 1
+           : kRsStagedSmemBudget / per_stage < 2 ? 2
+           : kRsStagedSmemBudget / per_stage > 8 ? 8
+                                                 : kRsStagedSmemBudget / per_stage;
 }
+
+// What the consumers of a stage need of its tile, written by thread 0 when
+// it issues the tile's copies: the consumers read it from shared memory
+// instead of searching the segment table and indexing the parameter block.
+struct StageTile {
+    int64_t fbase, sbase, len, unit_numel;
+    float *master, *m, *v;
+    uint16_t *pshard;
+    int32_t rank, base;
+};
+static_assert(sizeof(StageTile) == 72, "a compact stage descriptor");
 
 template <int RC, bool kGradBf16>
 struct RsStage {
     static constexpr int kEB = kGradBf16 ? 2 : 4;
-    static constexpr int kSlice = (int)kTile * kEB;  // one rank's slice of a tile
+    static constexpr int kVE = 16 / kEB;             // elements per 16-byte vector
+    static constexpr int kData = (int)kTile * kEB;   // one rank's elements of a tile
+    // A slice holds a tile's elements from the 16-byte boundary at or below
+    // its start to the one at or above its end (up to kVE - 1 elements more
+    // on each side); the realigning reads (below) stay inside it too.
+    static constexpr int kSlice = kData + 2 * kVE * kEB;
     static constexpr int kBytes = RC * kSlice;       // one stage
-    static constexpr bool kOn =
-        RC > 0 && RC * kEB >= kRsStageMinGradBytes && kBytes <= kRsStageMaxBytes;
-    static constexpr int stages() { return stages_for(kBytes); }
-    static constexpr size_t smem();
+    static constexpr bool kOn = RC > 0 && RC * kEB >= kRsStageMinGradBytes &&
+                                kBytes - 2 * RC * kVE * kEB <= kRsStageMaxBytes;
+    static constexpr int stages()
+    {
+        return stages_for(kBytes + (int)sizeof(uint64_t) + (int)sizeof(StageTile));
+    }
+    static constexpr size_t smem()
+    {
+        return (size_t)stages() * (kBytes + sizeof(uint64_t) + sizeof(StageTile));
+    }
 };
+
+// What a stage holds of tile T's gradient slices: the elements from
+// `first`, the 16-byte boundary at or below T.fbase (`lead` = T.fbase -
+// first), to the 16-byte boundary at or above the tile's end, but not past
+// the last whole vector of the gradient buffers (P = T.unit_numel elements,
+// 16-byte aligned bases); `nst` elements, `bytes` per rank. So the copies
+// stay inside the buffers, and only the unit's very last tile can leave a
+// few elements (those past the buffers' last whole vector) unstaged.
+struct StagedSpan {
+    int64_t first;
+    int lead;
+    int nst;
+    uint32_t bytes;
+};
+
+template <class S>
+__device__ __forceinline__ StagedSpan staged_span(const Tile &T)
+{
+    StagedSpan z;
+    z.first = T.fbase & ~(int64_t)(S::kVE - 1);
+    z.lead = (int)(T.fbase - z.first);
+    int64_t last = (T.fbase + T.len + S::kVE - 1) & ~(int64_t)(S::kVE - 1);
+    const int64_t cap = T.unit_numel & ~(int64_t)(S::kVE - 1);
+    if (last > cap)
+        last = cap;
+    z.nst = last > z.first ? (int)(last - z.first) : 0;
+    z.bytes = (uint32_t)z.nst * S::kEB;
+    return z;
+}
 
 template <bool kUnits, class PP>
 __device__ __forceinline__ Tile rs_tile(const PP &p, int64_t t)
@@ -907,11 +966,6 @@ __device__ __forceinline__ Tile rs_tile(const PP &p, int64_t t)
     if (!kUnits)
         T.base = 0;
     return T;
-}
-
-__device__ __forceinline__ bool vector_aligned(const Tile &T)
-{
-    return ((T.fbase | T.sbase) & (kElemsPerThread - 1)) == 0;
 }
 
 // The rank-ordered fold of the 8 staged gradient elements at tile offset e.
@@ -946,18 +1000,70 @@ __device__ __forceinline__ void fold8_staged(const unsigned char *st, int64_t e,
     }
 }
 
-// What the consumers of a stage need of its tile, written by thread 0 when
-// it issues the tile's copies: the consumers read it from shared memory
-// instead of searching the segment table and indexing the parameter block.
-struct StageTile {
-    Tile T;
-    RankPtrs b;
-};
+// The same fold for a tile that starts off a 16-byte boundary: the thread's
+// 8 elements begin at stage element i0 = lead + e, i0 * kEB bytes into each
+// slice, sh = that mod 16 being the same for every thread of the tile (A =
+// sh / 4 whole words, B = sh mod 4 bytes). Each slice is read with aligned
+// 16-byte loads covering the elements, and the words are shifted into place.
+// Elements at stage index nst and beyond (at the end of the unit, past the
+// buffers' last whole vector) were not copied; they are read from the
+// gradient buffers.
+template <int RC, bool kGradBf16, int A>
+__device__ __forceinline__ void fold8_realigned(const unsigned char *st, int64_t i0, int nst,
+                                                const void *const *grad, int64_t j, float acc[8])
+{
+    using S = RsStage<RC, kGradBf16>;
+    constexpr int kOut = 2 * S::kEB;               // words of 8 elements
+    constexpr int kChunks = (kOut + A + 1 + 3) / 4; // 16-byte loads that cover them
+    const int ob = (int)((i0 * S::kEB) & ~(int64_t)15);
+    const uint32_t bshift = 8u * (uint32_t)((i0 * S::kEB) & 3);
+#pragma unroll
+    for (int q = 0; q < RC; q++) {
+        const unsigned char *sl = st + q * S::kSlice + ob;
+        uint32_t w[4 * kChunks];
+#pragma unroll
+        for (int c = 0; c < kChunks; c++) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sl + 16 * c);
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+        }
+        uint32_t o[kOut];
+#pragma unroll
+        for (int m = 0; m < kOut; m++)
+            o[m] = __funnelshift_r(w[m + A], w[m + A + 1 < 4 * kChunks ? m + A + 1 : m + A],
+                                   bshift);
+        float g[8];
+        if (kGradBf16) {
+            unpack_bf16x8(make_uint4(o[0], o[1], o[2], o[3]), g);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                g[k] = __uint_as_float(o[k]);
+        }
+        if (i0 + 8 > nst) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (i0 + k >= nst)
+                    g[k] = load_grad<kGradBf16>(grad[q], j + k);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            acc[k] = q == 0 ? g[k] : __fadd_rn(acc[k], g[k]);
+    }
+}
 
 template <int RC, bool kGradBf16>
-constexpr size_t RsStage<RC, kGradBf16>::smem()
+__device__ __forceinline__ void fold8_staged_at(const unsigned char *st, int64_t i0, int nst,
+                                                const void *const *grad, int64_t j, float acc[8])
 {
-    return (size_t)stages() * (kBytes + sizeof(uint64_t) + sizeof(StageTile));
+    switch ((int)((i0 * RsStage<RC, kGradBf16>::kEB) & 15) >> 2) {
+    case 0: fold8_realigned<RC, kGradBf16, 0>(st, i0, nst, grad, j, acc); break;
+    case 1: fold8_realigned<RC, kGradBf16, 1>(st, i0, nst, grad, j, acc); break;
+    case 2: fold8_realigned<RC, kGradBf16, 2>(st, i0, nst, grad, j, acc); break;
+    default: fold8_realigned<RC, kGradBf16, 3>(st, i0, nst, grad, j, acc); break;
+    }
 }
 
 template <int RC, bool kGradBf16, bool kParamBf16, bool kUnits>
@@ -971,22 +1077,22 @@ __global__ void __launch_bounds__(kThreads, kRsStagedCtasPerSm)
     uint64_t *bar = reinterpret_cast<uint64_t *>(stage + (size_t)NS * S::kBytes);
     StageTile *desc = reinterpret_cast<StageTile *>(bar + NS);
     const int tid = threadIdx.x;
-    // thread 0: tile t's descriptor and gradient copies onto stage k (no
-    // copies for a misaligned tile: its phase completes at once)
+    // thread 0: tile t's descriptor and gradient copies onto stage k (a
+    // phase with no bytes completes at once)
     auto issue = [&](const Tile &T, int k) {
-        desc[k].T = T;
-        desc[k].b = rank_ptrs(p, T);
-        const uint32_t bytes =
-            vector_aligned(T) ? (uint32_t)((T.len * S::kEB) & ~(int64_t)15) : 0u;
-        mbar_arrive_expect_tx(&bar[k], bytes * RC);
-        if (bytes != 0) {
+        const RankPtrs b = rank_ptrs(p, T);
+        desc[k] = {T.fbase, T.sbase, T.len, T.unit_numel, b.master, b.m, b.v, b.pshard,
+                   T.rank, T.base};
+        const StagedSpan z = staged_span<S>(T);
+        mbar_arrive_expect_tx(&bar[k], z.bytes * RC);
+        if (z.bytes != 0) {
             unsigned char *dst = stage + (size_t)k * S::kBytes;
 #pragma unroll
             for (int q = 0; q < RC; q++)
                 bulk_load(dst + q * S::kSlice,
                           static_cast<const unsigned char *>(p.grad[T.base + q]) +
-                              T.fbase * S::kEB,
-                          bytes, &bar[k]);
+                              z.first * S::kEB,
+                          z.bytes, &bar[k]);
         }
     };
     if (tid == 0) {
@@ -1005,9 +1111,21 @@ __global__ void __launch_bounds__(kThreads, kRsStagedCtasPerSm)
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, i++) {
         const int k = (int)(i % NS);
         // written by thread 0 at least one barrier ago
-        const Tile T = desc[k].T;
-        const RankPtrs b = desc[k].b;
-        const bool vec = vector_aligned(T) && e + kElemsPerThread <= T.len;
+        const StageTile &d = desc[k];
+        Tile T;
+        T.fbase = d.fbase;
+        T.sbase = d.sbase;
+        T.len = d.len;
+        T.unit_numel = d.unit_numel;
+        T.rank = d.rank;
+        T.base = d.base;
+        T.nvalid = d.len;
+        const RankPtrs b = {p.grad + d.base, p.acc + d.base, d.master, d.m, d.v, d.pshard,
+                            p.gshard[d.base + d.rank]};
+        // shard offsets are multiples of 8 (segment starts are padded), so
+        // every full vector of a tile takes the vector path
+        const bool vec =
+            e + kElemsPerThread <= T.len && (T.sbase & (kElemsPerThread - 1)) == 0;
         const int64_t s = T.sbase + e;
         float4 w0, w1, m0, m1, v0, v1;
         if (vec) {
@@ -1026,11 +1144,21 @@ __global__ void __launch_bounds__(kThreads, kRsStagedCtasPerSm)
         const bool ok = mbar_wait_bounded(&bar[k], (uint32_t)((i / NS) & 1), kStageWaitNs);
         if (ok) {
             if (vec) {
+                const StagedSpan z = staged_span<S>(T);
+                const unsigned char *st = stage + (size_t)k * S::kBytes;
                 float acc[8];
-                fold8_staged<RC, kGradBf16>(stage + (size_t)k * S::kBytes, e, acc);
+                if (z.lead == 0 && e + kElemsPerThread <= z.nst)
+                    fold8_staged<RC, kGradBf16>(st, e, acc);
+                else
+                    fold8_staged_at<RC, kGradBf16>(st, z.lead + e, z.nst, b.grad, T.fbase + e,
+                                                   acc);
                 adamw8_store<kParamBf16>(p.c, b, s, acc, w0, w1, m0, m1, v0, v1);
             } else {
-                rs_adamw_tile<RC, kGradBf16, kParamBf16, false>(p, RC, T);
+                // the tile's last partial vector, element by element
+                const int64_t stop = e + kElemsPerThread < T.len ? e + kElemsPerThread : T.len;
+                for (int64_t q = e; q < stop; q++)
+                    rs_adamw_scalar<kGradBf16, kParamBf16, false>(b, p.c, RC, T.fbase + q,
+                                                                  T.sbase + q);
             }
         }
         // every thread is done with stage k; all learn whether a wait gave up
