@@ -800,6 +800,103 @@ __device__ __forceinline__ void adamw8_store(const AdamScalars &c, const RankPtr
     }
 }
 
+// Eight elements of kEB bytes that start A words plus bshift / 8 bytes into
+// the 16-byte chunks held in w[], widened to fp32: each output word is a
+// funnel shift of two neighbouring input words.
+template <int kEB, int A>
+struct Realign {
+    static constexpr int kOut = 2 * kEB;                    // words of 8 elements
+    static constexpr int kChunks = (kOut + A + 1 + 3) / 4;  // 16-byte chunks covering them
+    static __device__ __forceinline__ void to_f32(const uint32_t *w, uint32_t bshift, float g[8])
+    {
+        uint32_t o[kOut];
+#pragma unroll
+        for (int m = 0; m < kOut; m++)
+            o[m] = __funnelshift_r(w[m + A], w[m + A + 1 < 4 * kChunks ? m + A + 1 : m + A],
+                                   bshift);
+        if (kEB == 2) {
+            unpack_bf16x8(make_uint4(o[0], o[1], o[2], o[3]), g);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                g[k] = __uint_as_float(o[k]);
+        }
+    }
+};
+
+// The rank-ordered fold of the 8 gradient elements that start A words plus
+// bshift / 8 bytes past unit index cb (a 16-byte boundary), read from the
+// gradient buffers with aligned 16-byte loads. The caller checks that the
+// chunks lie inside the buffers.
+template <int RC, bool kGradBf16, int A>
+__device__ __forceinline__ void fold8_realigned_global(const void *const *grad, int64_t cb,
+                                                       uint32_t bshift, float acc[8])
+{
+    constexpr int kEB = kGradBf16 ? 2 : 4;
+    using RA = Realign<kEB, A>;
+#pragma unroll
+    for (int q = 0; q < RC; q++) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const unsigned char *>(grad[q]) + cb * kEB);
+        uint32_t w[4 * RA::kChunks];
+#pragma unroll
+        for (int c = 0; c < RA::kChunks; c++) {
+            const uint4 v = ld_stream(src + c);
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+        }
+        float g[8];
+        RA::to_f32(w, bshift, g);
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            acc[k] = q == 0 ? g[k] : __fadd_rn(acc[k], g[k]);
+    }
+}
+
+// A tile whose full-buffer start is off a 16-byte boundary (its shard start
+// is aligned): each thread takes its 8 consecutive elements as on the
+// vector path, reading the gradients with aligned 16-byte loads that it
+// realigns in registers. The threads' chunks overlap, so DRAM sees each
+// byte once. A thread whose chunks would pass the buffers' last whole vector
+// (only at the unit's end), and the tile's last partial vector, go element
+// by element.
+template <int RC, bool kGradBf16, bool kParamBf16>
+__device__ __forceinline__ void rs_adamw_tile_realigned(const AdamScalars &c, const RankPtrs &b,
+                                                        const Tile &T)
+{
+    constexpr int kEB = kGradBf16 ? 2 : 4;
+    constexpr int kVE = 16 / kEB;
+    constexpr int kMaxChunkElems = Realign<kEB, 3>::kChunks * kVE;
+    const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+    if (e >= T.len)
+        return;
+    const int64_t j = T.fbase + e;
+    const int64_t cb = j & ~(int64_t)(kVE - 1);
+    const int64_t cap = T.unit_numel & ~(int64_t)(kVE - 1);
+    if (e + kElemsPerThread > T.len || cb + kMaxChunkElems > cap) {
+        const int64_t stop = e + kElemsPerThread < T.len ? e + kElemsPerThread : T.len;
+        for (int64_t q = e; q < stop; q++)
+            rs_adamw_scalar<kGradBf16, kParamBf16, false>(b, c, RC, T.fbase + q, T.sbase + q);
+        return;
+    }
+    const int64_t s = T.sbase + e;
+    float4 w0 = ld_f4(b.master + s), w1 = ld_f4(b.master + s + 4);
+    float4 m0 = ld_f4(b.m + s), m1 = ld_f4(b.m + s + 4);
+    float4 v0 = ld_f4(b.v + s), v1 = ld_f4(b.v + s + 4);
+    const int sh = (int)(j - cb) * kEB;  // the same for every thread of the tile
+    const uint32_t bshift = 8u * (uint32_t)(sh & 3);
+    float acc[8];
+    switch (sh >> 2) {
+    case 0: fold8_realigned_global<RC, kGradBf16, 0>(b.grad, cb, bshift, acc); break;
+    case 1: fold8_realigned_global<RC, kGradBf16, 1>(b.grad, cb, bshift, acc); break;
+    case 2: fold8_realigned_global<RC, kGradBf16, 2>(b.grad, cb, bshift, acc); break;
+    default: fold8_realigned_global<RC, kGradBf16, 3>(b.grad, cb, bshift, acc); break;
+    }
+    adamw8_store<kParamBf16>(c, b, s, acc, w0, w1, m0, m1, v0, v1);
+}
+
 // One reduce-scatter + AdamW tile.
 template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, class PP>
 __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
@@ -819,6 +916,16 @@ __device__ __forceinline__ void rs_adamw_tile(const PP &p, int R, const Tile &T)
         b.grad = gl;
     }
     if (((T.fbase | T.sbase) & (kElemsPerThread - 1)) != 0) {
+        // bf16 gradients at R = 8 only (misaligned 7.4M-parameter unit: 0.0668
+        // -> 0.0597 ms). With fp32 gradients the scalar pairs below were as
+        // fast (the realigning loads fetch 48 bytes per 32 used); at R = 4 the
+        // extra code cost the L2-resident 3.1M-parameter block 2-4 %.
+        if constexpr (RC == 8 && !kAccum && kGradBf16) {
+            if ((T.sbase & (kElemsPerThread - 1)) == 0) {
+                rs_adamw_tile_realigned<RC, kGradBf16, kParamBf16>(p.c, b, T);
+                return;
+            }
+        }
         if constexpr (RC > 0) {
 #pragma unroll 1
             for (int k = 0; k < kElemsPerThread; k += 2) {
@@ -1013,8 +1120,7 @@ __device__ __forceinline__ void fold8_realigned(const unsigned char *st, int64_t
                                                 const void *const *grad, int64_t j, float acc[8])
 {
     using S = RsStage<RC, kGradBf16>;
-    constexpr int kOut = 2 * S::kEB;               // words of 8 elements
-    constexpr int kChunks = (kOut + A + 1 + 3) / 4; // 16-byte loads that cover them
+    constexpr int kChunks = Realign<S::kEB, A>::kChunks;
     const int ob = (int)((i0 * S::kEB) & ~(int64_t)15);
     const uint32_t bshift = 8u * (uint32_t)((i0 * S::kEB) & 3);
 #pragma unroll
@@ -1029,19 +1135,8 @@ __device__ __forceinline__ void fold8_realigned(const unsigned char *st, int64_t
             w[4 * c + 2] = v.z;
             w[4 * c + 3] = v.w;
         }
-        uint32_t o[kOut];
-#pragma unroll
-        for (int m = 0; m < kOut; m++)
-            o[m] = __funnelshift_r(w[m + A], w[m + A + 1 < 4 * kChunks ? m + A + 1 : m + A],
-                                   bshift);
         float g[8];
-        if (kGradBf16) {
-            unpack_bf16x8(make_uint4(o[0], o[1], o[2], o[3]), g);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; k++)
-                g[k] = __uint_as_float(o[k]);
-        }
+        Realign<S::kEB, A>::to_f32(w, bshift, g);
         if (i0 + 8 > nst) {
 #pragma unroll
             for (int k = 0; k < 8; k++)

@@ -92,6 +92,21 @@ def test_flat_units_with_misaligned_rank_pieces(cuda_lib):
                            prior_moments=True))
 
 
+@pytest.mark.parametrize("mode,shapes", [
+    ("flat", [(7_427_862,)]),                  # S odd: ranks 1-7 start off the 8-element grid
+    ("per_param", [(4097, 513), (1001, 63), (5,)]),
+])
+def test_register_kernel_realigned_tiles_vs_oracle(cuda_lib, mode, shapes):
+    """bf16 gradients at R = 8 on a launch too small to stage: the register
+    kernel reads misaligned tiles with aligned 16-byte loads and realigns
+    them in registers."""
+    P = sum(int(np.prod(s)) for s in shapes)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert -(-P // TILE) + 8 * len(shapes) < MIN_TILES_PER_CTA * CTAS_PER_SM * sms
+    run_unit_case(UnitCase(shapes=shapes, R=8, mode=mode, seed=90, step=2, outlier_frac=0.01,
+                           prior_moments=True))
+
+
 def test_bounded_wait_gives_up_and_the_device_stays_usable(cuda_lib):
     """The staged kernel's bounded wait, on an mbarrier that nothing
     completes: the block gives up, counts itself, and the device still runs
