@@ -9,11 +9,15 @@
 // persistent grid (a few CTAs per SM) walks the tiles in order, so at any
 // moment the grid touches one contiguous window of every buffer. A thread
 // owns 8 consecutive elements of a tile (16 in the gather): one 16-byte
-// vector per bf16 stream, two per fp32 stream. Tiles whose start is not
-// aligned in both the full and the shard buffer (ragged FSDP1 boundaries,
-// odd row widths) take a scalar path with the same per-element arithmetic.
-// The all-reduce and gradient-accumulation kernels tile the flat unit index
-// the same way.
+// vector per bf16 stream, two per fp32 stream. Shard offsets are always
+// multiples of 8 elements; a tile whose full-buffer start is not (ragged
+// FSDP1 boundaries, odd row widths) is realigned: the gather stages its
+// shard elements in shared memory, the staged reduce-scatter stages the
+// 16-byte span around it and the register one (bf16, R = 8) loads aligned
+// chunks, each shifting the words into place in registers; the other
+// register reduce-scatters take a scalar path with the same per-element
+// arithmetic. The all-reduce and gradient-accumulation kernels tile the flat
+// unit index the same way.
 //
 // Segment descriptors and the per-rank pointers travel in the kernel
 // parameter block (__grid_constant__), so the kernels need no device memory
