@@ -89,6 +89,51 @@ def test_two_threads_two_streams(cuda_lib):
     assert not errors, errors
 
 
+def test_two_threads_staged_units_match_a_serial_run(cuda_lib):
+    """Two host threads drive units large enough for the staged
+    reduce-scatter (21M parameters; R = 8 and R = 4, so two different staged
+    kernels) on their own streams at once, five steps each; every buffer
+    must equal a serial run of the same steps bit for bit."""
+    from fully_sharded_state_gb300 import AdamWHP, ShardedUnit, synth
+    hp = AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    shapes = [(4096, 4096), (1024, 4096), (4096,)]
+    dev = torch.device("cuda")
+
+    def run(R, stream):
+        with torch.cuda.stream(stream):
+            U = ShardedUnit(shapes, R)
+            U.shard_from_full(synth.device_normal(10 + R, U.P, 0.02, dev), stream=stream)
+            g = [synth.device_normal(20 + R + r, U.P, 1e-3, dev, torch.bfloat16)
+                 for r in range(R)]
+            full = U.alloc_full()
+            for _ in range(5):
+                U.all_gather(full, stream=stream)
+                U.reduce_scatter_adamw(g, hp, stream=stream)
+            U.all_gather(full, stream=stream)
+        stream.synchronize()
+        return [t.clone() for t in U.master + U.m + U.v + U.param_shard + full]
+
+    got, errors = {}, []
+
+    def work(R):
+        try:
+            got[R] = run(R, torch.cuda.Stream())
+        except Exception as e:  # surfaced to the main thread
+            errors.append(e)
+
+    ts = [threading.Thread(target=work, args=(R,)) for R in (8, 4)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+    for R in (8, 4):
+        want = run(R, torch.cuda.current_stream())
+        for a, b in zip(got[R], want):
+            assert torch.equal(bits(a), bits(b))
+
+
 @pytest.mark.parametrize("k", range(12))
 def test_random_units_per_call(cuda_lib, k):
     """Random groups of units through the multi-unit calls: 1 to 24 units
