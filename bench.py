@@ -79,8 +79,11 @@ def rs_kernel_name(shapes, R: int, grad_b: int, sms: int) -> str:
     unit: the staged one (gradient slices by cp.async.bulk) when the R
     gradient streams carry at least 8 bytes per element, a stage (R slices of
     a 2,048-element tile) fits in 32 KB and the launch has at least 32 tiles
-    per staged thread block (2 per SM); the register one otherwise."""
-    tiles = 0
+    per staged thread block (2 per SM), or 16 when at most half of its
+    elements sit in rank pieces that start on the 8-element grid; the
+    register one otherwise."""
+    tiles = elems = aligned8 = 0
+    full_off = 0
     for s in shapes:
         inner = 1
         for x in s[1:]:
@@ -89,8 +92,13 @@ def rs_kernel_name(shapes, R: int, grad_b: int, sms: int) -> str:
         for r in range(R):
             n = max(0, min(rows, s[0] - r * rows)) * inner
             tiles += -(-n // 2048)
+            elems += n
+            if (full_off + r * rows * inner) % 8 == 0:  # shard offsets are always
+                aligned8 += n
+        full_off += s[0] * inner
+    per_cta = 16 if 2 * aligned8 < elems else 32
     if (R in (2, 4, 8) and R * grad_b >= 8 and R * 2048 * grad_b <= 32 * 1024
-            and tiles >= 32 * 2 * sms):
+            and tiles >= per_cta * 2 * sms):
         return "rs_adamw_staged_kernel"
     return "rs_adamw_kernel"
 

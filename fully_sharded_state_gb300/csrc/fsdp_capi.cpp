@@ -59,7 +59,7 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
     LaunchPlan cur;
     for (Seg s : segs) {
         // owned elements and those in aligned rank pieces (see LaunchPlan)
-        int64_t elems = 0, aligned = 0;
+        int64_t elems = 0, aligned = 0, aligned8 = 0;
         const int pieces = s.owner >= 0 ? 1 : R;
         for (int r = 0; r < pieces; r++) {
             int64_t n = s.owner >= 0 ? s.numel : s.numel - (int64_t)r * s.rank_stride;
@@ -68,6 +68,8 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
             elems += n;
             if (start % align == 0 && s.shard_off % align == 0)
                 aligned += n;
+            if (start % 8 == 0 && s.shard_off % 8 == 0)
+                aligned8 += n;
         }
         int64_t tiles;
         if (s.owner >= 0) {
@@ -95,6 +97,7 @@ std::vector<LaunchPlan> make_plans(const std::vector<Seg> &segs, int R, bool pad
         cur.total_tiles += tiles;
         cur.elems += elems;
         cur.aligned_elems += aligned;
+        cur.aligned8_elems += aligned8;
         cur.segs.push_back(s);
     }
     if (!cur.segs.empty())

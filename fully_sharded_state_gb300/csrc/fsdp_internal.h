@@ -51,6 +51,8 @@ struct LaunchPlan {
     int64_t total_tiles = 0;
     int64_t elems = 0;
     int64_t aligned_elems = 0;
+    int64_t aligned8_elems = 0;  // those whose full and shard starts are multiples
+                                 // of 8 elements (the reduce-scatter's vectors)
 };
 
 // AdamW scalars, formed on the host in double and rounded once to fp32.

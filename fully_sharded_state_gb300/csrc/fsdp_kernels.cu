@@ -70,6 +70,12 @@ constexpr int kRsStagedSmemBudget = 97 * 1024;
 //   R x gradient bytes = 4 (bf16 R = 2): 1.08-1.3 at every size.
 constexpr int kRsStageMinGradBytes = 8;
 constexpr int kRsStagedMinTilesPerCta = 32;
+// A launch whose elements mostly sit in rank pieces that start off the
+// 8-element grid stages from 16 tiles per CTA: the staged kernel realigns
+// them at full speed, while the register kernel's scalar path is slow
+// (misaligned flat units, 5,859 tiles, staged / register: bf16 R = 4 0.87,
+// bf16 R = 8 0.93, fp32 R = 4 0.86; 2,929 tiles: bf16 R = 4 1.06).
+constexpr int kRsStagedMinTilesPerCtaMisaligned = 16;
 // all-gather (256 threads, 16 elements per thread): 1/SM 0.613 ms,
 // 2/SM 0.668 ms, 3/SM 0.667 ms on a Llama unit, whose tiles are full and
 // aligned. A launch whose elements mostly sit in misaligned or partial tiles
@@ -1673,6 +1679,7 @@ std::vector<Launch> plan_launches(int n, const fsdp_layout_t *const *Ls, Plans p
             cur.merged.total_tiles += pl.total_tiles;
             cur.merged.elems += pl.elems;
             cur.merged.aligned_elems += pl.aligned_elems;
+            cur.merged.aligned8_elems += pl.aligned8_elems;
         }
     }
     if (!cur.units.empty())
@@ -1788,7 +1795,7 @@ fsdp_status launch_all_gather(int n, const fsdp_layout_t *const *Ls, const void 
 // accumulators are read and the launch gives every staged CTA at least
 // kRsStagedMinTilesPerCta tiles; the register kernel otherwise.
 template <int RC, bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
-static fsdp_status rs_run(int dev, RsParams &p, cudaStream_t s)
+static fsdp_status rs_run(int dev, RsParams &p, cudaStream_t s, int min_tiles_per_cta)
 {
     using S = RsStage<RC, kGradBf16>;
     if constexpr (!kAccum && S::kOn) {
@@ -1798,7 +1805,7 @@ static fsdp_status rs_run(int dev, RsParams &p, cudaStream_t s)
                                   p.total_tiles, kRsStagedCtasPerSm, &grid, S::smem());
         if (st != FSDP_OK)
             return st;
-        if (p.total_tiles >= (int64_t)kRsStagedMinTilesPerCta * grid) {
+        if (p.total_tiles >= (int64_t)min_tiles_per_cta * grid) {
             kernel<<<grid, kThreads, S::smem(), s>>>(p);
             return check_launch("rs_adamw_staged");
         }
@@ -1808,28 +1815,31 @@ static fsdp_status rs_run(int dev, RsParams &p, cudaStream_t s)
 }
 
 template <bool kGradBf16, bool kParamBf16, bool kAccum, bool kUnits>
-static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s)
+static fsdp_status rs_dispatch(int dev, int R, RsParams &p, cudaStream_t s, int mt)
 {
     switch (R) {
-    case 2: return rs_run<2, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
-    case 4: return rs_run<4, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
-    case 8: return rs_run<8, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
-    default: return rs_run<0, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s);
+    case 2: return rs_run<2, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s, mt);
+    case 4: return rs_run<4, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s, mt);
+    case 8: return rs_run<8, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s, mt);
+    default: return rs_run<0, kGradBf16, kParamBf16, kAccum, kUnits>(dev, p, s, mt);
     }
 }
 
 // Accumulating launches always hold one unit.
 template <bool kAccum, bool kUnits>
-static fsdp_status rs_dispatch_dtypes(int dev, const fsdp_layout_t *L, RsParams &p, cudaStream_t s)
+static fsdp_status rs_dispatch_dtypes(int dev, const fsdp_layout_t *L, RsParams &p, cudaStream_t s,
+                                      const LaunchPlan &pl)
 {
+    const int mt = 2 * pl.aligned8_elems < pl.elems ? kRsStagedMinTilesPerCtaMisaligned
+                                                    : kRsStagedMinTilesPerCta;
     const bool gb = L->grad_dtype == FSDP_BF16, pb = L->param_dtype == FSDP_BF16;
     if (gb && pb)
-        return rs_dispatch<true, true, kAccum, kUnits>(dev, L->R, p, s);
+        return rs_dispatch<true, true, kAccum, kUnits>(dev, L->R, p, s, mt);
     if (gb)
-        return rs_dispatch<true, false, kAccum, kUnits>(dev, L->R, p, s);
+        return rs_dispatch<true, false, kAccum, kUnits>(dev, L->R, p, s, mt);
     if (pb)
-        return rs_dispatch<false, true, kAccum, kUnits>(dev, L->R, p, s);
-    return rs_dispatch<false, false, kAccum, kUnits>(dev, L->R, p, s);
+        return rs_dispatch<false, true, kAccum, kUnits>(dev, L->R, p, s, mt);
+    return rs_dispatch<false, false, kAccum, kUnits>(dev, L->R, p, s, mt);
 }
 
 fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *const *grad,
@@ -1858,11 +1868,11 @@ fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *c
         bind(p.gshard, grad_shard_out, l, R);
         fill_segs(p, l.get());
         if (acc)
-            st = rs_dispatch_dtypes<true, false>(ds.device(), L, p, s);
+            st = rs_dispatch_dtypes<true, false>(ds.device(), L, p, s, l.get());
         else if (l.units.size() > 1)
-            st = rs_dispatch_dtypes<false, true>(ds.device(), L, p, s);
+            st = rs_dispatch_dtypes<false, true>(ds.device(), L, p, s, l.get());
         else
-            st = rs_dispatch_dtypes<false, false>(ds.device(), L, p, s);
+            st = rs_dispatch_dtypes<false, false>(ds.device(), L, p, s, l.get());
         if (st != FSDP_OK)
             return st;
     }

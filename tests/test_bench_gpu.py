@@ -77,6 +77,8 @@ def test_peak_memory_matches_the_pages_formula(cuda_lib):
 @pytest.mark.parametrize("shapes,R,gdt", [
     ([(4096, 4096), (1024, 4096), (4096,)], 8, "bf16"),  # staged
     ([(6000, 4097)], 4, "f32"),                           # staged, fp32 gradients
+    ([(11996, 1001)], 4, "bf16"),                         # staged from 16 tiles a CTA:
+                                                          # 3 of 4 rank pieces misaligned
     ([(512, 512), (512,)], 4, "bf16"),                    # too few tiles: register
     ([(6000, 4097)], 2, "bf16"),                          # 4 gradient bytes: register
     ([(6000, 4097)], 8, "f32"),                           # a 64 KB stage: register

@@ -58,6 +58,10 @@ def test_rs_kernel_name_follows_the_staging_rule():
     # the bar: 32 tiles x 2 thread blocks x SMs
     assert bench.rs_kernel_name([(9728 * 2048,)], 4, 2, 152) == "rs_adamw_staged_kernel"
     assert bench.rs_kernel_name([(9724 * 2048,)], 4, 2, 152) == "rs_adamw_kernel"
+    # 16 tiles when most rank pieces start off the 8-element grid: rows of
+    # 2,999 x 1,001 put ranks 1-3 off it (5,864 tiles)
+    assert bench.rs_kernel_name([(11996, 1001)], 4, 2, 152) == "rs_adamw_staged_kernel"
+    assert bench.rs_kernel_name([(5996, 1001)], 4, 2, 152) == "rs_adamw_kernel"
 
 
 def test_max_over_ranks_two_gloo_ranks():
