@@ -179,7 +179,8 @@ typedef struct {
  * not needed for training). step >= 1; 0 <= beta1, beta2 < 1; eps > 0.
  * For R = 4 or 8 (bf16 gradients) and R = 2 or 4 (fp32 gradients), on
  * launches of at least ~10,000 tiles of 2,048 elements (units of ~20M
- * parameters and up), the kernel stages the gradient slices in shared memory
+ * parameters and up; ~5,000 tiles when most rank pieces start off the
+ * 8-element grid), the kernel stages the gradient slices in shared memory
  * with bulk copies and waits for them at most ~2 s; see
  * fsdp_stage_wait_timeouts. The results are the same either way. */
 fsdp_status fsdp_reduce_scatter_adamw(const fsdp_layout_t *layout, const void *const *grad_full,
