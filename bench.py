@@ -724,9 +724,21 @@ def run_ours(args):
     ar_out = [torch.empty(U0.P, dtype=torch.float32, device=dev) for _ in range(R)]
     ar_ms = timed_launches(torch, stream,
                            lambda: U0.all_reduce(grads[0], ar_out, "f32", stream=stream))
-    del ar_out
     ddp = entry("all_reduce_kernel (DDP all-reduce: bf16 grads -> fp32 outputs)",
                 R * U0.P * (2 + 4), ar_ms, "all_reduce")
+    # ZeRO-1's step on the same unit: the all-reduce above, each rank's AdamW
+    # from its own averaged fp32 gradient, then the all-gather
+    z1_ms = timed_launches(torch, stream,
+                           lambda: U0.adamw_from_reduced(ar_out, hp, stream=stream))
+    del ar_out
+    z1_adamw = entry("adamw_reduced_kernel (ZeRO-1: AdamW on each rank's partition from the "
+                     "all-reduced gradient)", U0.P * (4 + 24 + 2), z1_ms, None)
+    zero1 = {"adamw_from_reduced": z1_adamw,
+             "step_ms_per_unit": round(ar_ms + z1_ms + statistics.mean(ag_ms), 4),
+             "fsdp_step_ms_per_unit": round(statistics.mean(rs_ms) + statistics.mean(ag_ms), 4),
+             "algorithmic_bytes_per_param": {"zero1": 48 + 30 + 18, "fsdp": 42 + 18},
+             "note": "all-reduce + AdamW from the averaged gradient + all-gather, against "
+                     "the fused reduce-scatter + AdamW + all-gather; same results bit for bit"}
 
     # gradient accumulation on the same unit: one more micro-batch added into
     # the fp32 accumulators, and the last micro-batch fused into the step
@@ -802,6 +814,7 @@ def run_ours(args):
                 "pct_of_hbm_peak": round(value / world / peak, 4),
                 "pct_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "roofline_all_gather": roofline_ag, "ddp_all_reduce": ddp,
+                "zero1": zero1,
                 "grad_accumulation": accumulation, "pack": pack, "ceilings": ceilings,
                 "configs": configs, "peak_memory": memory,
                 "clocks": clocks.summary(), "gpu_launches": launches,

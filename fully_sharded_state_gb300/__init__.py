@@ -8,6 +8,7 @@ HBM. The compute path is the CUDA library ``_lib/libfsdp_shard.so``
 """
 from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, FSDP_ZERO3, AdamWHP, FsdpError,
                    FsdpArgumentError, LibraryNotBuilt, fsdp_accumulate_grad,
+                   fsdp_adamw_from_reduced,
                    fsdp_all_gather_unflatten, fsdp_all_gather_unflatten_units, fsdp_all_reduce,
                    fsdp_reduce_scatter_adamw_accum, fsdp_layout, fsdp_pack_flat,
                    fsdp_reduce_scatter_adamw, fsdp_reduce_scatter_adamw_gather,
@@ -17,7 +18,7 @@ from .capi import (FSDP_BF16, FSDP_F32, FSDP_FLAT, FSDP_PER_PARAM, FSDP_ZERO3, A
                    prepare_fsdp_reduce_scatter_adamw, prepare_fsdp_reduce_scatter_adamw_units)
 
 __all__ = ["FSDP_BF16", "FSDP_F32", "FSDP_FLAT", "FSDP_PER_PARAM", "FSDP_ZERO3", "AdamWHP", "FsdpError",
-           "FsdpArgumentError", "LibraryNotBuilt", "fsdp_accumulate_grad",
+           "FsdpArgumentError", "LibraryNotBuilt", "fsdp_accumulate_grad", "fsdp_adamw_from_reduced",
            "fsdp_all_gather_unflatten", "fsdp_all_gather_unflatten_units", "fsdp_all_reduce",
            "fsdp_reduce_scatter_adamw_accum", "fsdp_layout", "fsdp_pack_flat",
            "fsdp_reduce_scatter_adamw", "fsdp_reduce_scatter_adamw_gather",

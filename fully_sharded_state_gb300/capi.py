@@ -108,6 +108,9 @@ def load(path: str = LIB_PATH):
     L.fsdp_write_stream.restype = ctypes.c_int
     L.fsdp_write_stream.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int64,
                                     ctypes.c_uint32, _vp]
+    L.fsdp_adamw_from_reduced.restype = ctypes.c_int
+    L.fsdp_adamw_from_reduced.argtypes = [_vp] + [ctypes.POINTER(_vp)] * 5 + [
+        ctypes.POINTER(AdamWHP), ctypes.c_int64, _vp]
     L.fsdp_stage_wait_timeouts.restype = ctypes.c_int
     L.fsdp_stage_wait_timeouts.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint64)]
     L.fsdp_stage_wait_selftest.restype = ctypes.c_int
@@ -315,6 +318,20 @@ def fsdp_reduce_scatter_adamw_gather(layout: Layout, grad_full, master, m, v, pa
     _check(load().fsdp_reduce_scatter_adamw_gather(
         layout.handle, *arrs, ctypes.byref(hp), int(step), gather_layout.handle, sh, fo,
         _stream_handle(stream)))
+
+
+def fsdp_adamw_from_reduced(layout: Layout, grad_avg_full, master, m, v, param_shard_out,
+                            hp: AdamWHP, step: int, stream=None) -> None:
+    """ZeRO-1's step: AdamW on each rank's own elements from its full,
+    already averaged fp32 gradient (fsdp_all_reduce's fp32 output)."""
+    R, P, S = layout.R, layout.full_numel, layout.shard_numel
+    a = _Args()
+    arrs = (a.array(grad_avg_full, R, "grad_avg_full", P, FSDP_F32),
+            a.array(master, R, "master", S, FSDP_F32), a.array(m, R, "m", S, FSDP_F32),
+            a.array(v, R, "v", S, FSDP_F32),
+            a.array(param_shard_out, R, "param_shard_out", S, FSDP_BF16, allow_none=True))
+    _check(load().fsdp_adamw_from_reduced(layout.handle, *arrs, ctypes.byref(hp), int(step),
+                                          _stream_handle(stream)))
 
 
 def fsdp_all_reduce(layout: Layout, grad_full, out, out_dtype: int, stream=None) -> None:

@@ -602,6 +602,38 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
                                   adam_scalars(hp, step, L->R), G, shard, full_out, stream);
 }
 
+fsdp_status fsdp_adamw_from_reduced(const fsdp_layout_t *L, const float *const *grad_avg_full,
+                                    float *const *master, float *const *m, float *const *v,
+                                    void *const *param_shard_out, const fsdp_adamw_hp *hp,
+                                    int64_t step, void *stream)
+{
+    if (L == nullptr)
+        return set_error(FSDP_EINVAL, "fsdp_adamw_from_reduced: layout is NULL");
+    fsdp_status st = check_hp(hp, step);
+    if (st != FSDP_OK || L->P == 0)
+        return st;
+    std::vector<Span> spans;
+    const int64_t sb = L->shard_numel * 4;
+    if ((st = check_ptrs((const void *const *)grad_avg_full, L->R, L->P * 4, false,
+                         "grad_avg_full", &spans)) != FSDP_OK ||
+        (st = check_ptrs((const void *const *)master, L->R, sb, true, "master", &spans)) !=
+            FSDP_OK ||
+        (st = check_ptrs((const void *const *)m, L->R, sb, true, "m", &spans)) != FSDP_OK ||
+        (st = check_ptrs((const void *const *)v, L->R, sb, true, "v", &spans)) != FSDP_OK)
+        return st;
+    if (L->param_dtype == FSDP_BF16) {
+        if ((st = check_ptrs((const void *const *)param_shard_out, L->R, L->shard_numel * 2, true,
+                             "param_shard_out", &spans)) != FSDP_OK)
+            return st;
+    } else if (param_shard_out != nullptr) {
+        return set_error(FSDP_EINVAL, "param_shard_out must be NULL for an F32 layout");
+    }
+    if ((st = check_spans(spans)) != FSDP_OK)
+        return st;
+    return launch_adamw_reduced(L, grad_avg_full, master, m, v, param_shard_out,
+                                adam_scalars(hp, step, L->R), stream);
+}
+
 fsdp_status fsdp_all_reduce(const fsdp_layout_t *L, const void *const *grad_full,
                             void *const *out, fsdp_dtype out_dtype, void *stream)
 {

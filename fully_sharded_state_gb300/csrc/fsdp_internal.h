@@ -84,6 +84,9 @@ fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *c
                             const AdamScalars &c, void *stream, const float *const *acc);
 fsdp_status launch_accumulate(const fsdp_layout_t *L, float *const *acc, const void *const *grad,
                               int first, void *stream);
+fsdp_status launch_adamw_reduced(const fsdp_layout_t *L, const float *const *grad_avg,
+                                 float *const *master, float *const *m, float *const *v,
+                                 void *const *param_shard_out, const AdamScalars &c, void *stream);
 fsdp_status launch_all_reduce(const fsdp_layout_t *L, const void *const *grad, void *const *out,
                               fsdp_dtype out_dtype, void *stream);
 fsdp_status launch_write_stream(void *const *dst, int n, int64_t bytes, uint32_t pattern,

@@ -21,7 +21,7 @@
 //
 // Segment descriptors and the per-rank pointers travel in the kernel
 // parameter block (__grid_constant__), so the kernels need no device memory
-// beyond the caller's buffers (and one counter of abandoned waits, below).
+// beyond the caller's buffers (and two counters of abandoned waits, below).
 //
 // The fused reduce-scatter + AdamW brings each tile's R gradient slices into
 // shared memory with cp.async.bulk, a few tiles ahead, on per-stage
@@ -1285,6 +1285,49 @@ __global__ void __launch_bounds__(kThreads, kRsStagedCtasPerSm)
     }
 }
 
+// ------------------------------------------ AdamW from a reduced gradient ----
+//
+// ZeRO-1's update: the gradients were all-reduced already, so every rank's
+// full buffer holds the averaged fp32 gradient, and rank r updates the
+// elements it owns from its own buffer: no sum, and the scalars' inv_R is 1
+// (an exact multiply). The same tiles and AdamW epilogue as the fused
+// reduce-scatter, so with the all-reduce's output the results are the fused
+// kernel's bit for bit.
+template <bool kParamBf16>
+__global__ void __launch_bounds__(kThreads) adamw_reduced_kernel(const __grid_constant__ RsParams p)
+{
+    const int64_t e = (int64_t)threadIdx.x * kElemsPerThread;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const Tile T = locate<kTile>(p.seg, p.nseg, t, false);  // one unit: base 0
+        if (e >= T.len)
+            continue;
+        const RankPtrs b = rank_ptrs(p, T);
+        const float *g = static_cast<const float *>(p.grad[T.rank]);
+        const int64_t s = T.sbase + e;
+        if (((T.fbase & 3) | (T.sbase & 3)) == 0 && e + kElemsPerThread <= T.len) {
+            const int64_t j = T.fbase + e;
+            const float4 g0 = ld_f4(g + j), g1 = ld_f4(g + j + 4);
+            float4 w0 = ld_f4(b.master + s), w1 = ld_f4(b.master + s + 4);
+            float4 m0 = ld_f4(b.m + s), m1 = ld_f4(b.m + s + 4);
+            float4 v0 = ld_f4(b.v + s), v1 = ld_f4(b.v + s + 4);
+            float acc[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            adamw8_store<kParamBf16>(p.c, b, s, acc, w0, w1, m0, m1, v0, v1);
+        } else {
+            const int64_t stop = e + kElemsPerThread < T.len ? e + kElemsPerThread : T.len;
+            for (int64_t q = e; q < stop; q++) {
+                const int64_t sq = T.sbase + q;
+                const float gq = __fmul_rn(__ldcs(g + T.fbase + q), p.c.inv_R);
+                const AdamOut o = adamw_elem(p.c, gq, b.master[sq], b.m[sq], b.v[sq]);
+                b.master[sq] = o.w;
+                b.m[sq] = o.m;
+                b.v[sq] = o.v;
+                if (kParamBf16)
+                    b.pshard[sq] = f32_to_bf16_bits(o.w);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------- gradient accumulation ----
 //
 // acc[q] = g[q] (first micro-batch) or acc[q] + g[q], fp32, for every rank
@@ -1873,6 +1916,39 @@ fsdp_status launch_rs_adamw(int n, const fsdp_layout_t *const *Ls, const void *c
             st = rs_dispatch_dtypes<false, true>(ds.device(), L, p, s, l.get());
         else
             st = rs_dispatch_dtypes<false, false>(ds.device(), L, p, s, l.get());
+        if (st != FSDP_OK)
+            return st;
+    }
+    return FSDP_OK;
+}
+
+fsdp_status launch_adamw_reduced(const fsdp_layout_t *L, const float *const *grad_avg,
+                                 float *const *master, float *const *m, float *const *v,
+                                 void *const *param_shard_out, const AdamScalars &c, void *stream)
+{
+    DeviceScope ds;
+    fsdp_status st = ds.enter(master[0]);
+    if (st != FSDP_OK)
+        return st;
+    RsParams p;
+    memset(&p, 0, sizeof p);
+    p.R = L->R;
+    p.c = c;
+    p.c.inv_R = 1.0f;  // the gradient is averaged already
+    for (int r = 0; r < L->R; r++) {
+        p.grad[r] = grad_avg[r];
+        p.master[r] = master[r];
+        p.m[r] = m[r];
+        p.v[r] = v[r];
+        p.pshard[r] = param_shard_out ? static_cast<uint16_t *>(param_shard_out[r]) : nullptr;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    for (const LaunchPlan &pl : L->valid_plans) {
+        fill_segs(p, pl);
+        st = L->param_dtype == FSDP_BF16
+                 ? run(ds.device(), adamw_reduced_kernel<true>, p, s, "adamw_reduced", kRsCtasPerSm)
+                 : run(ds.device(), adamw_reduced_kernel<false>, p, s, "adamw_reduced",
+                       kRsCtasPerSm);
         if (st != FSDP_OK)
             return st;
     }

@@ -107,6 +107,16 @@ class ShardedUnit:
         (fp32 or bf16), for comparison with the sharded path."""
         capi.fsdp_all_reduce(self.layout, grads, out, _DT[out_dtype][0], stream)
 
+    def adamw_from_reduced(self, grad_avg_full, hp: capi.AdamWHP, step: int | None = None,
+                           stream=None) -> None:
+        """ZeRO-1's optimizer step: every rank updates its own elements from
+        its full averaged fp32 gradient (all_reduce's fp32 output). The step
+        count advances as with reduce_scatter_adamw."""
+        t = self._next_step(step)
+        capi.fsdp_adamw_from_reduced(self.layout, grad_avg_full, self.master, self.m, self.v,
+                                     self.param_shard, hp, t, stream)
+        self.step = t
+
     # -- prepared calls (checked once, re-issued every step) -----------------
     def prepare_all_gather(self, full_out):
         """The all-gather into ``full_out`` with its arguments bound; call the

@@ -206,6 +206,22 @@ fsdp_status fsdp_reduce_scatter_adamw_gather(
     const fsdp_adamw_hp *hp, int64_t step, const fsdp_layout_t *G, const void *const *shard,
     void *const *full_out, void *stream);
 
+/* ZeRO-1's optimizer step ("从源码理解 FSDP", §1.2, the ZeRO stages: the
+ * gradients are all-reduced, so every rank holds the whole averaged
+ * gradient, and each rank updates only the parameters and optimizer state of
+ * its own partition, which an all-gather then shares). grad_avg_full[r]:
+ * rank r's full averaged fp32 gradient, P elements, as fsdp_all_reduce with
+ * an FSDP_F32 output leaves it. For each element that rank r owns, with j its
+ * unit index: g = grad_avg_full[r][j], then the AdamW update of
+ * fsdp_reduce_scatter_adamw on master/m/v[r] and param_shard_out[r] (BF16
+ * layouts only, else NULL). With fsdp_all_reduce's output the results equal
+ * fsdp_reduce_scatter_adamw's on the same gradients bit for bit. Errors: as
+ * fsdp_reduce_scatter_adamw. */
+fsdp_status fsdp_adamw_from_reduced(const fsdp_layout_t *layout, const float *const *grad_avg_full,
+                                    float *const *master, float *const *m, float *const *v,
+                                    void *const *param_shard_out, const fsdp_adamw_hp *hp,
+                                    int64_t step, void *stream);
+
 /* All-reduce, the DDP collective that FSDP is compared against ("FSDP
  * Training Step Walkthrough", per-step communication summary; "FSDP2 的参数
  * 全聚合、梯度归约分片与显存峰值", §01 and §09). Every rank d receives, for

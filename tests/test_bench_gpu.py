@@ -30,8 +30,10 @@ def test_bench_line_contract(cuda_lib, capsys):
     assert len(e2e["h2d_link_GBps_before_after"]) == 2
     assert all(x > 0 for x in e2e["h2d_link_GBps_before_after"])
     assert "workload" in line["config"]
+    z1 = line["zero1"]
+    assert z1["step_ms_per_unit"] > z1["fsdp_step_ms_per_unit"] > 0
     for entry in (line["roofline_all_gather"], line["ddp_all_reduce"], line["pack"],
-                  *line["grad_accumulation"].values()):
+                  z1["adamw_from_reduced"], *line["grad_accumulation"].values()):
         assert entry["achieved"] > 0
         assert entry["frac_of_nominal"] < entry["frac"]
     ceil = line["ceilings"]

@@ -213,6 +213,31 @@ def test_reduce_scatter_adamw_rejects_bad_arguments(lib, over, status):
     assert lib.fsdp_last_error()
 
 
+def _call_adamw_reduced(lib, L, a):
+    return lib.fsdp_adamw_from_reduced(L.handle if L else None, a["grad"], a["master"], a["m"],
+                                       a["v"], a["pshard"], ctypes.byref(a["hp"]), a["step"],
+                                       None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(step=0), capi.FSDP_EINVAL),
+    (dict(hp=_hp(beta1=1.0)), capi.FSDP_EINVAL),
+    (dict(grad=None), capi.FSDP_EINVAL),
+    (dict(grad=_ptrs([BASE, 0])), capi.FSDP_EINVAL),
+    (dict(master=_ptrs([BASE + 10 * (1 << 20) + 4, BASE + 11 * (1 << 20)])), capi.FSDP_EALIGN),
+    (dict(pshard=None), capi.FSDP_EINVAL),
+    # master[1] overlaps m[0]
+    (dict(master=_ptrs([BASE + 10 * (1 << 20), BASE + 20 * (1 << 20) + 64])), capi.FSDP_EINVAL),
+    # v[0] overlaps an averaged gradient (an input)
+    (dict(v=_ptrs([BASE + 64, BASE + 31 * (1 << 20)])), capi.FSDP_EINVAL),
+])
+def test_adamw_from_reduced_rejects_bad_arguments(lib, over, status):
+    L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(4096, 16)], capi.FSDP_BF16, capi.FSDP_BF16)
+    assert _call_adamw_reduced(lib, L, _rs_args(**over)) == status
+    assert lib.fsdp_last_error()
+    assert _call_adamw_reduced(lib, None, _rs_args()) == capi.FSDP_EINVAL
+
+
 def test_f32_layouts_take_no_bf16_shard(lib):
     L = capi.fsdp_layout(capi.FSDP_PER_PARAM, 2, [(4096, 16)], capi.FSDP_F32, capi.FSDP_F32)
     assert _call_rs(lib, L, _rs_args()) == capi.FSDP_EINVAL

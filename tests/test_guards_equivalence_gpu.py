@@ -3,7 +3,8 @@
 Guards: every output buffer sits inside a larger allocation whose bytes
 before and after it hold a known pattern; after pack, gather, reduce-scatter
 + AdamW (with and without accumulators, register and staged kernels),
-all-reduce and accumulation the patterns must be intact, so no kernel writes
+all-reduce, ZeRO-1's AdamW from the averaged gradient and accumulation the
+patterns must be intact, so no kernel writes
 outside its buffers.
 
 Equivalence ("FSDP2 的参数全聚合、梯度归约分片与显存峰值", §12): one sharded
@@ -74,6 +75,7 @@ def test_kernels_write_only_inside_their_buffers(cuda_lib, mode, pdt, gdt, R, sh
     U.reduce_scatter_adamw_accum(acc, grads, hp)
     ar = [G(P, torch.float32) for _ in range(R)]
     U.all_reduce(grads, ar, "f32")
+    U.adamw_from_reduced(ar, hp)
     ar16 = [G(P, torch.bfloat16) for _ in range(R)]
     U.all_reduce(grads, ar16, "bf16")
     G.check()
